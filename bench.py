@@ -1,0 +1,359 @@
+"""Decode-step benchmark: tokens/s and us/token of the captured step on GB300,
+achieved HBM bandwidth against the roofline, the fp64 oracle timed beside it.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 8b] [--impl ours|reference]
+
+One step = one replay of the whole captured decode step (embedding, every
+layer's norm/QKV/RoPE/KV-write/attention/O-proj/norm/SwiGLU MLP, final norm,
+LM head, greedy argmax) over one batch of `rows` tokens.  value = tokens/s with
+the slot records already in device memory (one device-to-device slot copy and
+one graph launch per step); e2e = the same through dec_step with host buffers
+(slot write host->device, launch, id + non-finite flag readback, bounded wait).
+With --gpus N > 1 (torchrun) every rank runs an independent replica: the path
+does not shard, so there is no collective on the data path.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode tokens/s and µs/token at 1 GB300; achieved HBM GB/s vs roofline"
+PROFILE = os.path.join(ROOT, "profiles", "gemv_gate_up_8b.md")
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _describe(wl, positions):
+    lay = "paged KV (%d-token pages, pool %d)" % (wl.page_size, wl.num_pages) if wl.layout == "paged" \
+        else "contiguous KV"
+    return (f"{wl.name}: {wl.n_layers} layers, d_model {wl.d_model}, {wl.n_heads} q / {wl.n_kv_heads} kv heads "
+            f"x {wl.head_dim}, SwiGLU {wl.ffn_hidden}, vocab {wl.vocab}, {wl.wdtype} weights, {lay}, "
+            f"cap {wl.cap}, rows {wl.rows}, pos per step cycling {positions}")
+
+
+def _positions(wl):
+    import gen
+    if wl.positions and len(wl.positions) == wl.rows:
+        return [[int(p) for p in wl.positions]]                       # one record: fixed per-row positions
+    if wl.positions:
+        return [[int(p)] * wl.rows for p in wl.positions]              # cycle the listed positions
+    return [[int(p) for p in gen.row_positions(wl)]]
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str):
+        self.uuid = uuid
+        self.proc = None
+        self.out = os.path.join("/tmp", f"clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.out, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", self.uuid, f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.out):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _traffic_from_profile():
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary,
+    or None if the summary is missing or the kernel source changed since."""
+    try:
+        txt = open(PROFILE).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    h = re.search(r"gemv_source_sha256:\s*([0-9a-f]+)", txt)
+    if not m or not h:
+        return None
+    src = open(os.path.join(ROOT, "graph_replay_gb300", "csrc", "gemv.cu"), "rb").read()
+    if hashlib.sha256(src).hexdigest() != h.group(1):
+        return None
+    return float(m.group(1))
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import gen
+    from gen.device import place_kv, to_tensor
+    from graph_replay_gb300 import Decoder, make_config
+    from graph_replay_gb300 import _binding as B
+
+    torch.cuda.set_device(local_rank)
+    dev = f"cuda:{local_rank}"
+    wl = gen.WORKLOADS[args.workload]
+    # weights: drawn from the seeded generator tensor by tensor, uploaded, host copy dropped
+    w = {"layers": []}
+    mw = gen.make_weights(wl) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
+    if mw is not None:
+        from gen.device import upload_weights
+        w = upload_weights(mw, dev)
+    else:
+        from gen.workloads import _draw, LAYER_ROLES
+        for g in ("embed", "final_norm", "lm_head"):
+            w[g] = to_tensor(_draw(wl, g, 0xFFFF), dev)
+        for l in range(wl.n_layers):
+            w["layers"].append({r: to_tensor(_draw(wl, r, l), dev) for r in LAYER_ROLES})
+    cfg = make_config(wl.n_layers, wl.d_model, wl.n_heads, wl.n_kv_heads, wl.head_dim, wl.ffn_hidden, wl.vocab,
+                      wl.wdtype, wl.kvdtype, wl.rms_eps, wl.rope_theta, device=local_rank)
+    dec = Decoder(cfg, w, cap=wl.cap, rows=wl.rows, kv_layout=wl.layout, page_size=wl.page_size,
+                  num_pages=wl.num_pages)
+    slot_map = None
+    if wl.layout == "paged":
+        slot_map = gen.slot_map(wl)
+        dec.set_slot_map(slot_map)
+    plist = _positions(wl)
+    maxpos = max(max(p) for p in plist)
+    # KV pre-filled N(0,1) up to the largest position each row is stepped at
+    for r in range(wl.rows):
+        npos = max(p[r] for p in plist)
+        for l in range(wl.n_layers):
+            for which in (0, 1):
+                place_kv(dec.kv(l, which), gen.kv_prefill(wl, l, which, r, npos), r, 0, slot_map, wl.page_size)
+    toks = gen.ints(wl.seed, 0x51, 0, wl.vocab, wl.rows * len(plist)).reshape(len(plist), wl.rows)
+    recs = []
+    for i, p in enumerate(plist):
+        wm = [int(slot_map[r][p[r] // wl.page_size]) * wl.page_size + p[r] % wl.page_size for r in range(wl.rows)] \
+            if slot_map is not None else [0] * wl.rows
+        recs.append(list(toks[i]) + list(p) + wm)
+    dev_slots = torch.tensor(recs, dtype=torch.int32, device=dev)   # [n_records, 3*rows]
+    stream = dec.stream()
+    st = dec.stats()
+    kernels = st["kernels_per_step"]
+
+    def step(i):
+        dec.launch(dev_slots[i % len(recs)])
+
+    # ---- device-resident throughput ----
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    uuid = str(getattr(torch.cuda.get_device_properties(local_rank), "uuid", ""))
+    clocks = Clocks(uuid if uuid.startswith("GPU-") else "GPU-" + uuid)
+    clocks.start()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ms = e0.elapsed_time(e1)
+    clk = clocks.stop()
+    res = dec.wait()   # the device checks of the timed steps passed
+    assert res.nonfinite.sum() == 0
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / args.steps
+    tok_s = world * wl.rows * args.steps / (ms / 1e3)
+
+    # ---- end to end through dec_step with host buffers ----
+    host_recs = [(np.array(r[:wl.rows], np.int32), np.array(r[wl.rows:2 * wl.rows], np.int32),
+                  np.array(r[2 * wl.rows:], np.int32) if slot_map is not None else None) for r in recs]
+    for i in range(args.warmup):
+        t_, p_, w_ = host_recs[i % len(recs)]
+        dec.step(t_, p_, w_, logits=False)
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        t_, p_, w_ = host_recs[i % len(recs)]
+        dec.step(t_, p_, w_, logits=False)
+    e2e_s = time.perf_counter() - t0
+    if world > 1:
+        t = torch.tensor([e2e_s], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e_tok_s = world * wl.rows * args.steps / e2e_s
+
+    # ---- dominant kernel alone: RMSNorm + gate/up GEMV, cycling the layers ----
+    hbm_peak, peak_kind = _peaks()
+    n_k = max(2 * wl.n_layers, 32)
+    idx = [4 + 5 * (i % wl.n_layers) for i in range(n_k)]
+    for i in idx[:4]:
+        B.dec_launch_kernel(dec.h, i)
+    k0 = torch.cuda.Event(enable_timing=True)
+    k1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    k0.record(stream)
+    kbytes = 0
+    for i in idx:
+        kbytes = B.dec_launch_kernel(dec.h, i)
+    k1.record(stream)
+    torch.cuda.synchronize()
+    k_us = k0.elapsed_time(k1) * 1e3 / len(idx)
+    k_gbs = kbytes / (k_us * 1e-6) / 1e9
+    traffic = _traffic_from_profile() if wl.name == "8b" else None
+
+    step_bytes = wl.step_bytes()
+    step_gbs = step_bytes / (ms_step * 1e-3) / 1e9
+    out = {
+        "metric": METRIC, "value": round(tok_s, 3), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "us_per_token": round(ms_step * 1e3 / wl.rows, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.wdtype, "data": "synthetic",
+        "config": {"workload": _describe(wl, [p for p in plist]), "rows": wl.rows, "cap": wl.cap,
+                   "kv_layout": wl.layout, "parallelism": f"replicas{world}",
+                   "l2": "inputs larger than L2 (weights %.2f GB per step)" % (wl.weight_bytes() / 1e9),
+                   "step": "1 D2D slot copy + 1 graph launch (%d kernels)" % kernels},
+        "roofline": {"bound": "hbm", "kernel": "RMSNorm+gate/up GEMV (per layer)", "achieved": round(k_gbs, 1),
+                     "peak": hbm_peak, "unit": "GB/s", "frac": round(k_gbs / hbm_peak, 4),
+                     "traffic": traffic, "bytes_per_launch": kbytes, "us_per_launch": round(k_us, 3),
+                     "peak_kind": peak_kind},
+        "step_roofline": {"bytes_per_step": step_bytes, "achieved_gbs": round(step_gbs, 1),
+                          "frac_of_measured": round(step_gbs / hbm_peak, 4),
+                          "frac_of_8tbs": round(step_gbs / 8000.0, 4),
+                          "weight_bytes": wl.weight_bytes(), "kv_swept_bytes": wl.kv_swept_bytes()},
+        "e2e": {"value": round(e2e_tok_s, 3), "unit": "tokens/s",
+                "us_per_token": round(e2e_s / args.steps * 1e6 / wl.rows, 3),
+                "h2d_bytes_per_step": 3 * 4 * wl.rows, "d2h_bytes_per_step": 104,
+                "readback": "greedy ids + non-finite flags + error word"},
+        "gpu_launches": kernels * args.steps,
+        "graph_launches_per_step": 1,
+        "clocks": clk,
+    }
+    if mw is not None and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(wl, mw, plist, toks, seconds=args.cpu_seconds)
+    dec.close()
+    return out
+
+
+def cpu_baseline(wl, mw, plist, toks, seconds=20.0, steps_cap=None):
+    """The fp64 oracle as it stands, on this host's cores, over a bounded sample
+    of the same workload (same weights, pre-filled KV, positions, tokens)."""
+    import gen
+    import oracle
+    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    orcs = []
+    for r in range(wl.rows):
+        o = oracle.Oracle(mw, cap=wl.cap, rows=1)
+        npos = max(p[r] for p in plist)
+        for l in range(wl.n_layers):
+            o.K[0][l][:npos] = gen.kv_prefill(wl, l, 0, r, npos)
+            o.V[0][l][:npos] = gen.kv_prefill(wl, l, 1, r, npos)
+        orcs.append(o)
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        p = plist[n % len(plist)]
+        for r in range(wl.rows):
+            orcs[r].step(0, int(toks[n % len(plist)][r]), int(p[r]))
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or (steps_cap and n >= steps_cap):
+            break
+    return {"value": round(wl.rows * n / el, 5), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} fp64 oracle decode steps of the {wl.name} workload ({wl.rows} rows, same positions and "
+                      f"pre-filled KV), {el:.1f} s"}
+
+
+def run_reference(args):
+    import gen
+    wl = gen.WORKLOADS[args.workload]
+    mw = gen.make_weights(wl)
+    plist = _positions(wl)
+    toks = gen.ints(wl.seed, 0x51, 0, wl.vocab, wl.rows * len(plist)).reshape(len(plist), wl.rows)
+    # warm-up steps are part of the bounded sample budget: W short steps, then K timed
+    budget = max(5.0, min(120.0, args.cpu_seconds))
+    cpu_baseline(wl, mw, plist, toks, seconds=0.0, steps_cap=max(1, min(args.warmup, 2)))
+    cb = cpu_baseline(wl, mw, plist, toks, seconds=budget, steps_cap=args.steps)
+    return {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "tokens/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": _describe(wl, plist), "rows": wl.rows, "cap": wl.cap, "kv_layout": wl.layout},
+            "cpu_baseline": cb, "e2e": {"value": cb["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                                        "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="8b")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    import torch
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl", device_id=torch.device(f"cuda:{local_rank}"))
+    out = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,116 @@
+// internal.h -- launch interface between the engine (engine.cu) and the
+// kernel translation units.  Host-side only; no torch types anywhere.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace gd {
+
+// Raise a kernel's dynamic shared-memory cap to the device's opt-in limit
+// minus its static shared memory.  The cap is per function and shared by every
+// handle in the process, so it is raised once to the limit rather than set to
+// one plan's size (a smaller later value would break an earlier plan).
+inline cudaError_t raise_smem_cap(const void* fn) {
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, fn);
+    if (e != cudaSuccess) return e;
+    int dev = 0, optin = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess) return e;
+    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - (int)fa.sharedSizeBytes);
+}
+
+enum WType { W_F32 = 0, W_BF16 = 1 };
+
+// ---------------- fused norm + GEMV ----------------
+// out[r, n] (=|+=) sum_k W[n, k] * a[r, k] for the rows n of up to three
+// weight segments stacked in one output index space (e.g. Wq;Wk;Wv).
+// The activation a is built in shared memory by the prologue:
+//   PRO_PLAIN   a = act
+//   PRO_RMSNORM a = act / sqrt(mean(act^2) + eps) * gain
+//   PRO_SWIGLU  a = silu(act[:, :K]) * act[:, K:2K]
+enum Prologue { PRO_PLAIN = 0, PRO_RMSNORM = 1, PRO_SWIGLU = 2 };
+// Epilogue: store, add into out (residual), or store logits + greedy argmax.
+enum Epilogue { EPI_STORE = 0, EPI_ADD = 1, EPI_LOGITS = 2 };
+
+struct GemvParams {
+    const void* w[3];
+    int seg_rows[3];
+    int N;                 // total output rows
+    int K;                 // reduction length
+    int R;                 // activation rows in use (<= the kernel's NR)
+    const float* act;      // [R, act_stride] fp32
+    int act_stride;
+    const void* gain;      // [K] in the weight dtype (PRO_RMSNORM)
+    float eps;
+    float* out;            // [R, out_stride] fp32
+    int out_stride;
+    unsigned long long* amax;  // [R] argmax keys (EPI_LOGITS)
+    unsigned* nonfinite;       // [R] flags (EPI_LOGITS)
+    int rows_per_cta;
+};
+
+struct GemvPlan {
+    int wtype, pro, epi, nr;
+    int grid, block;
+    size_t smem;
+    GemvParams p;
+};
+
+// Fill plan->grid/block/smem/nr and p.rows_per_cta for the given shape.
+cudaError_t gemv_plan(GemvPlan* plan, int num_sms);
+cudaError_t gemv_launch(const GemvPlan& plan, cudaStream_t s, bool pdl);
+
+// ---------------- split-KV masked decode attention ----------------
+struct AttnParams {
+    const float* qkv;      // [R, qkv_stride]: q [Hq*hd], k [Hkv*hd], v [Hkv*hd] (fp32, pre-RoPE)
+    int qkv_stride;
+    void* Kc;              // this layer's K store (layout per `paged`)
+    void* Vc;
+    const int* pos;        // [R] slot
+    const int* slot_map;   // [R, pages_per_row] slot (paged)
+    const int* write_map;  // [R] slot (paged)
+    const float2* rope;    // [cap, hd/2] (cos, sin)
+    int cap, R, Hq, Hkv, hd;
+    int split_len, nsplit;
+    int page_size, pages_per_row, num_pages;
+    float* part;           // [R, Hq, nsplit, hd + 2] partial (m, l, o)
+    unsigned* counters;    // [R, Hkv] split-completion counters (zero between steps)
+    float* out;            // [R, Hq * hd]
+    unsigned* err;
+    float scale;
+};
+
+struct AttnPlan {
+    int kvtype;   // W_F32 / W_BF16
+    bool paged;
+    int group;    // Hq / Hkv
+    dim3 grid;
+    int block;
+    size_t smem;
+    AttnParams p;
+};
+
+// choose split_len / nsplit; returns cudaErrorInvalidValue for unsupported head_dim / group
+cudaError_t attn_plan(AttnPlan* plan, int num_sms);
+cudaError_t attn_launch(const AttnPlan& plan, cudaStream_t s, bool pdl);
+size_t attn_part_floats(int R, int Hq, int hd, int nsplit);
+
+// ---------------- embedding gather + per-step resets ----------------
+struct EmbedParams {
+    const void* E;         // [V, d] weight dtype
+    const int* tok;        // [R]
+    const int* pos;        // [R]
+    int R, V, d, cap;
+    float* x;              // [R, d]
+    unsigned* err;
+    unsigned long long* amax;
+    unsigned* nonfinite;
+};
+cudaError_t embed_launch(int wtype, const EmbedParams& p, cudaStream_t s);
+
+// a kernel that spins for about `ns` nanoseconds on one SM, then returns
+cudaError_t busy_launch(long long ns, cudaStream_t s);
+
+}  // namespace gd

@@ -1,0 +1,65 @@
+// misc.cu -- the step's first kernel (slot checks, per-step resets, embedding
+// gather) and a self-limiting busy kernel used to exercise the bounded wait.
+#include "common.cuh"
+#include "internal.h"
+
+namespace gd {
+
+// First kernel of every step.  One CTA, so the resets it makes are ordered
+// before its own checks, and every later kernel of the step runs after it.
+//   * clears the error word, the argmax keys and the non-finite flags;
+//   * checks Token[r] in [0, V) and Pos[r] in [0, cap), setting error bits
+//     ("Execution", section "Failure handling": a failing kernel check sets a
+//     bit in a reserved error word and the dispatch continues; the step's
+//     result is then discarded) -- an out-of-range token reads row 0 instead;
+//   * x[r, :] = E[Token[r], :] widened to fp32.
+template <typename WT>
+__global__ void __launch_bounds__(256) k_embed(const EmbedParams p) {
+    const int tid = threadIdx.x;
+    if (tid == 0) *p.err = 0u;
+    if (tid < p.R) {
+        p.amax[tid] = 0ull;
+        p.nonfinite[tid] = 0u;
+    }
+    __syncthreads();
+    const WT* E = reinterpret_cast<const WT*>(p.E);
+    for (int r = 0; r < p.R; ++r) {
+        int tok = p.tok[r];
+        const int pos = p.pos[r];
+        if (tok < 0 || tok >= p.V) {
+            if (tid == 0) atomicOr(p.err, FAULT_TOKEN);
+            tok = 0;
+        }
+        if ((pos < 0 || pos >= p.cap) && tid == 0) atomicOr(p.err, FAULT_POS);
+        const WT* e = E + (size_t)tok * p.d;
+        float* x = p.x + (size_t)r * p.d;
+        for (int i = tid; i < p.d; i += blockDim.x) x[i] = Elem<WT>::load1(e + i);
+    }
+}
+
+cudaError_t embed_launch(int wtype, const EmbedParams& p, cudaStream_t s) {
+    if (wtype == W_BF16)
+        k_embed<__nv_bfloat16><<<1, 256, 0, s>>>(p);
+    else
+        k_embed<float><<<1, 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+// Spins on the global nanosecond timer for `ns`, with an iteration cap as a
+// second bound, then returns: a kernel that is slow on purpose but always ends.
+__global__ void k_busy(long long ns) {
+    unsigned long long t0, t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    for (long long it = 0; it < (1ll << 26); ++it) {
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+        if ((long long)(t - t0) >= ns) break;
+        __nanosleep(1000);
+    }
+}
+
+cudaError_t busy_launch(long long ns, cudaStream_t s) {
+    k_busy<<<1, 32, 0, s>>>(ns);
+    return cudaGetLastError();
+}
+
+}  // namespace gd

@@ -1,0 +1,267 @@
+/*
+ * graphdec.h -- C ABI of the captured, constant-shape decode step on one GPU.
+ *
+ * What the library does.  A Llama-style pre-norm decoder step (embedding;
+ * per layer RMSNorm, QKV projection, RoPE, K/V write at the slot position,
+ * attention that sweeps the fixed KV capacity `cap` under an iota-vs-pos mask,
+ * output projection, RMSNorm, SwiGLU MLP; final RMSNorm, LM head, greedy
+ * argmax) is recorded once into a CUDA graph and replayed per token.  Between
+ * replays the host only rewrites the slot buffers (Token, Pos, and for paged
+ * KV the SlotMap page table and the WriteMap target slot).  Sources on the
+ * pages: "Execution" (sections "Why capture", "A constant-shape decode graph",
+ * "Slot buffers", "Per backend" -- PTX row, "Failure handling"),
+ * "Backends" (section "PTX (NVIDIA)"), "Models, Registry and the Driver"
+ * (sections "The Model" -- StepShape, "Shared components" -- standard_stack).
+ *
+ * Conventions shared by every call.
+ *   - Every call returns an int status (dec_status); DEC_OK == 0.  After a
+ *     failure, dec_last_error() returns a NUL-terminated message owned by the
+ *     handle (valid until the next call on that handle); dec_last_error(NULL)
+ *     gives the message of the last failed dec_init on the calling thread.
+ *   - Pointers marked "device" are CUDA device addresses on the handle's GPU;
+ *     "host" pointers are ordinary (pageable or pinned) host memory.  The
+ *     library never frees memory it did not allocate.
+ *   - A handle is thread-compatible, not thread-safe: one thread at a time.
+ *     All device work of a handle runs on one CUDA stream.
+ *   - Row-major everywhere.  Matrices use the nn.Linear layout [out, in].
+ *   - Failure states ("Execution", section "Failure handling"): a device-side
+ *     check that fails (token, position or map value out of range) sets a bit
+ *     in the step's error word; the step's results are discarded, the call
+ *     returns DEC_E_DEVICE_FAULT and the handle needs dec_reset_state() before
+ *     it steps again (DEC_E_NEEDS_RESET until then).  A CUDA error or a wait
+ *     that outlasts the configured timeout poisons the handle: every later
+ *     call except dec_last_error / dec_stats / dec_destroy returns
+ *     DEC_E_POISONED without touching the device.
+ */
+#ifndef GRAPHDEC_H
+#define GRAPHDEC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DEC_ABI_VERSION 1
+
+typedef struct dec_handle dec_handle;
+
+typedef enum dec_status {
+    DEC_OK = 0,
+    DEC_E_INVALID = 1,       /* malformed argument or configuration */
+    DEC_E_UNSUPPORTED = 2,   /* well-formed, but this library cannot run it (message names the field) */
+    DEC_E_RANGE = 3,         /* a token, position or map entry outside its range (host check) */
+    DEC_E_STATE = 4,         /* call out of order (e.g. dec_step before dec_capture) */
+    DEC_E_CUDA = 5,          /* CUDA runtime error; the handle is poisoned */
+    DEC_E_OOM = 6,           /* device allocation failed or workspace too small */
+    DEC_E_DEVICE_FAULT = 7,  /* a device-side check failed; see dec_stats.last_fault */
+    DEC_E_NEEDS_RESET = 8,   /* an earlier step failed; call dec_reset_state */
+    DEC_E_POISONED = 9,      /* the handle saw a CUDA error or a timeout; only dec_destroy helps */
+    DEC_E_TIMEOUT = 10       /* a device wait outlasted wait_timeout_ms; the handle is poisoned */
+} dec_status;
+
+/* bits of the device error word (dec_stats.last_fault) */
+#define DEC_FAULT_TOKEN     0x1u  /* Token[r] outside [0, vocab) */
+#define DEC_FAULT_POS       0x2u  /* Pos[r] outside [0, cap) */
+#define DEC_FAULT_WRITE_MAP 0x4u  /* WriteMap[r] outside [0, num_pages * page_size) */
+#define DEC_FAULT_SLOT_MAP  0x8u  /* a SlotMap entry outside [0, num_pages) */
+
+typedef enum dec_dtype { DEC_DTYPE_F32 = 0, DEC_DTYPE_BF16 = 1 } dec_dtype;
+
+/* KV layouts ("Execution", section "A constant-shape decode graph"):
+ *   CONTIGUOUS: per layer K and V of shape [rows, n_kv_heads, cap, head_dim];
+ *               the step writes position Pos[r] (a DynamicUpdateSlice).
+ *   PAGED:      per layer a pool [num_pages, n_kv_heads, page_size, head_dim]
+ *               for K and one for V; logical position j of row r lives in
+ *               slot SlotMap[r][j / page_size] * page_size + j % page_size, and
+ *               the step scatters the new K/V to slot WriteMap[r]
+ *               (a ScatterUpdate through Slot::WriteMap). */
+typedef enum dec_kv_layout { DEC_KV_CONTIGUOUS = 0, DEC_KV_PAGED = 1 } dec_kv_layout;
+
+/* Model configuration.  RMSNorm is x / sqrt(mean(x^2) + rms_eps) * g; RoPE is
+ * the half-split rotation of pairs (i, i + head_dim/2) by pos * rope_theta^(-2i/head_dim);
+ * attention scale is 1/sqrt(head_dim); q head i reads kv head i / (n_heads / n_kv_heads). */
+typedef struct dec_config {
+    int32_t n_layers;
+    int32_t d_model;
+    int32_t n_heads;        /* query heads */
+    int32_t n_kv_heads;     /* key/value heads; must divide n_heads */
+    int32_t head_dim;       /* even */
+    int32_t ffn_hidden;     /* SwiGLU hidden width */
+    int32_t vocab;
+    int32_t weight_dtype;   /* dec_dtype of every weight (matrices, embeddings, norm gains) */
+    int32_t kv_dtype;       /* dec_dtype of the stored K/V */
+    int32_t device;         /* CUDA device ordinal */
+    double rms_eps;
+    double rope_theta;
+    int64_t wait_timeout_ms;  /* bound on every device wait; <= 0 means 600000 (600 s) */
+} dec_config;
+
+/* Weight roles ("Execution": load_weights binds each weight by its typed role;
+ * a weight no binding names stays unbound and dec_capture refuses to run). */
+typedef enum dec_role {
+    DEC_W_EMBED = 0,       /* [vocab, d_model]                     global (layer = -1) */
+    DEC_W_ATTN_NORM = 1,   /* [d_model]                            per layer */
+    DEC_W_Q = 2,           /* [n_heads * head_dim, d_model]        per layer */
+    DEC_W_K = 3,           /* [n_kv_heads * head_dim, d_model]     per layer */
+    DEC_W_V = 4,           /* [n_kv_heads * head_dim, d_model]     per layer */
+    DEC_W_O = 5,           /* [d_model, n_heads * head_dim]        per layer */
+    DEC_W_FFN_NORM = 6,    /* [d_model]                            per layer */
+    DEC_W_GATE = 7,        /* [ffn_hidden, d_model]                per layer */
+    DEC_W_UP = 8,          /* [ffn_hidden, d_model]                per layer */
+    DEC_W_DOWN = 9,        /* [d_model, ffn_hidden]                per layer */
+    DEC_W_FINAL_NORM = 10, /* [d_model]                            global */
+    DEC_W_LM_HEAD = 11,    /* [vocab, d_model]                     global */
+    DEC_W_NROLES = 12
+} dec_role;
+
+typedef struct dec_weight {
+    int32_t role;      /* dec_role */
+    int32_t layer;     /* 0 .. n_layers-1 for per-layer roles, -1 for global roles */
+    int32_t dtype;     /* must equal dec_config.weight_dtype */
+    int32_t reserved;  /* 0 */
+    int64_t rows;      /* shape [rows, cols]; a gain vector of length n is [n, 1] */
+    int64_t cols;
+    const void *data;  /* device, 16-byte aligned, borrowed: must outlive the handle */
+} dec_weight;
+
+typedef struct dec_stats {
+    int64_t steps;            /* completed dec_step / dec_wait calls */
+    int64_t replays;          /* graph launches */
+    int64_t eager_steps;      /* kernel sequences launched without the graph */
+    int32_t kernels_per_step; /* kernel launches recorded per step */
+    int32_t graph_nodes;      /* nodes of the instantiated graph */
+    int32_t attn_splits;      /* KV splits per (row, kv head) */
+    int32_t attn_split_len;   /* positions per split */
+    uint32_t last_fault;      /* error word of the last failed step (DEC_FAULT_* bits) */
+    int32_t state;            /* 0 ready, 1 needs reset, 2 poisoned */
+    int32_t captured;         /* 1 after dec_capture */
+    int32_t rows;
+    int32_t cap;
+    int32_t kv_layout;
+    double last_step_us;      /* host wall time of the last dec_step */
+    int64_t workspace_bytes;  /* device bytes the capture uses (KV included) */
+    int64_t kv_bytes;         /* device bytes of K and V over all layers */
+} dec_stats;
+
+/* Create a handle for `cfg` on cfg->device.  Validates the configuration
+ * (DEC_E_INVALID / DEC_E_UNSUPPORTED naming the field) before touching the GPU.
+ * *out receives the handle, or NULL on failure. */
+int dec_init(const dec_config *cfg, dec_handle **out);
+
+/* Bind `n` weights by role ("Execution": load_weights(store, map)).  May be
+ * called several times before dec_capture; a later binding of the same
+ * (role, layer) replaces the earlier one.  Shapes and dtypes are checked
+ * against the configuration (DEC_E_INVALID).  The library reads the weights in
+ * place: nothing is copied. */
+int dec_load_weights(dec_handle *h, const dec_weight *w, size_t n);
+
+/* Device bytes that dec_capture needs for this shape (KV store, slots,
+ * activations, attention partials, RoPE table). */
+int dec_workspace_size(const dec_config *cfg, int32_t cap, int32_t rows, int32_t kv_layout,
+                       int32_t page_size, int32_t num_pages, size_t *bytes);
+
+/* Allocate the step's buffers, run the kernel sequence once eagerly (checks),
+ * clear the state, and record the sequence into one CUDA graph that serves
+ * every position 0 <= pos < cap ("Execution", section "A constant-shape decode
+ * graph": grids and buffer addresses stay constant, so one capture serves
+ * every position up to cap).  One capture per handle ("Models, Registry and
+ * the Driver": one entry per step shape; capacity is part of the shape).
+ *   cap        KV capacity (positions per row), >= 1
+ *   rows       sequences stepped together, 1 .. 8
+ *   kv_layout  dec_kv_layout
+ *   page_size, num_pages  paged layout only (cap % page_size == 0,
+ *              rows * cap / page_size <= num_pages); ignored for contiguous
+ *   workspace  device buffer of >= dec_workspace_size bytes, 256-byte aligned,
+ *              owned by the caller and kept until dec_destroy; NULL: the library
+ *              allocates (and frees at dec_destroy)
+ *   stream     cudaStream_t to run on; NULL: the library creates its own.
+ *              The legacy default stream cannot be captured and is refused.
+ * All bound weights must be present (DEC_E_INVALID names the first missing). */
+int dec_capture(dec_handle *h, int32_t cap, int32_t rows, int32_t kv_layout, int32_t page_size,
+                int32_t num_pages, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Rewrite the paged read map ("Execution", section "Slot buffers":
+ * Slot::SlotMap).  map: host, [rows, cap / page_size] int32 page ids, each in
+ * [0, num_pages) (DEC_E_RANGE otherwise).  Takes effect from the next step.
+ * DEC_E_STATE for a contiguous capture. */
+int dec_set_slot_map(dec_handle *h, const int32_t *map);
+
+/* One decode step of every row ("Execution", section "Per backend", PTX row:
+ * write slots, launch the graph, copy results back, wait).
+ *   tokens     host [rows], each in [0, vocab)
+ *   pos        host [rows], each in [0, cap): the absolute position of the token
+ *   write_map  host [rows] target slot for paged KV, or NULL to derive it from
+ *              the slot map as SlotMap[r][pos/page]*page + pos%page; ignored
+ *              for contiguous KV
+ *   logits_out host [rows, vocab] fp32, or NULL
+ *   ids_out    host [rows] greedy token ids (largest logit, lowest index on
+ *              ties), or NULL
+ *   nonfinite_out host [rows], 1 if any logit of the row is NaN or Inf, or NULL
+ * Host-side range checks return DEC_E_RANGE before anything is launched. */
+int dec_step(dec_handle *h, const int32_t *tokens, const int32_t *pos, const int32_t *write_map,
+             float *logits_out, int32_t *ids_out, uint8_t *nonfinite_out);
+
+/* Asynchronous half of a step: copy the slot record (device, [3 * rows]
+ * int32: tokens, then positions, then write map) into the slot buffers and
+ * launch the step, without waiting and without host-side range checks (the
+ * device checks still run).  Results stay on the device until dec_wait. */
+int dec_launch(dec_handle *h, const int32_t *dev_slots);
+
+/* Wait (bounded by wait_timeout_ms) for the launched steps and copy the last
+ * step's results back; any pointer may be NULL.  Returns DEC_E_DEVICE_FAULT if
+ * the last step's error word is non-zero. */
+int dec_wait(dec_handle *h, float *logits_out, int32_t *ids_out, uint8_t *nonfinite_out);
+
+/* 1: later steps launch the recorded kernel sequence directly on the stream
+ * instead of replaying the graph (same kernels, same arguments); 0: replay. */
+int dec_set_eager(dec_handle *h, int32_t eager);
+
+/* Zero the KV store, the slot buffers and the error word, and clear the
+ * needs-reset state ("Execution", section "Failure handling": step refuses
+ * until reset_state clears it).  A poisoned handle stays poisoned. */
+int dec_reset_state(dec_handle *h);
+
+/* Device address and byte size of one layer's K (which = 0) or V (which = 1)
+ * store, in the layout of the capture's dec_kv_layout; for tests that pre-fill
+ * or inspect the carried state. */
+int dec_kv_ptr(dec_handle *h, int32_t layer, int32_t which, void **ptr, size_t *bytes);
+
+/* Device address of the logits [rows, vocab] fp32 of the last step. */
+int dec_logits_ptr(dec_handle *h, float **ptr);
+
+/* The CUDA stream the handle runs on (as a cudaStream_t). */
+int dec_stream(dec_handle *h, void **stream);
+
+int dec_stats_get(const dec_handle *h, dec_stats *out);
+
+/* Profiling hook: launch kernel `index` of the recorded step sequence alone,
+ * eagerly, on the handle's stream (no slot write, no wait).  Order: 0 embedding;
+ * per layer l: 1+5l RMSNorm+QKV, 2+5l attention (RoPE, K/V write, combine),
+ * 3+5l output projection + residual, 4+5l RMSNorm+gate/up, 5+5l SwiGLU+down +
+ * residual; last (5L+1) final RMSNorm + LM head + argmax.  The kernel reads and
+ * writes the step's buffers as in a step (it changes the state).
+ * pdl: 1 launches with the programmatic-serialization attribute as in the
+ * graph, 0 with plain stream order.  *bytes (optional) receives the
+ * algorithmic bytes one launch moves (weights read once + activations, or the
+ * cap-swept K/V + q + partials for attention). */
+int dec_launch_kernel(dec_handle *h, int32_t index, int32_t pdl, int64_t *bytes);
+
+/* Test hook for the bounded wait: enqueue a kernel that busies one SM for
+ * about `microseconds` (clamped to [0, 2000000]) and then ends by itself. */
+int dec_debug_busy(dec_handle *h, int64_t microseconds);
+
+/* Test hook: change the wait bound of an existing handle (ms, > 0). */
+int dec_set_timeout(dec_handle *h, int64_t wait_timeout_ms);
+
+const char *dec_last_error(const dec_handle *h);
+const char *dec_status_str(int status);
+
+/* Free everything the library allocated (after a bounded wait for the stream). */
+int dec_destroy(dec_handle *h);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GRAPHDEC_H */

@@ -1,0 +1,241 @@
+"""GPU parity: the captured decode step against the fp64 oracle, through the C ABI.
+
+Tolerances ("Execution", section "Verification", tiers 1-2): integer and
+movement work bit-exact (KV write addresses, paged maps, capture versus eager,
+greedy ids where the oracle's top-2 margin exceeds 0.05); logits and the
+carried KV state within max-abs 2e-2 and relative L2 5e-3 for bf16 weights
+with fp32 accumulation, and within 1e-4 relative for the fp32 tiny model.
+"""
+import numpy as np
+import pytest
+
+import gen
+import oracle
+from _harness import assert_close, assert_greedy, kv_as_float, make_decoder
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_sequence(wl, n_prompt, n_decode, mw=None, check_kv=True, rows=None):
+    """Prompt stepped token by token, then greedy decode fed with the oracle's pick."""
+    from gen.device import read_kv
+    dec, mw = make_decoder(wl, mw)
+    orc = oracle.Oracle(mw, cap=wl.cap)
+    toks = list(gen.prompt_tokens(wl, n=n_prompt))
+    strict = 0
+    pos = 0
+    for i in range(n_prompt + n_decode):
+        t = toks[i]
+        res = dec.step([t], [pos])
+        ref = orc.step(0, t, pos)
+        assert_close(res.logits[0], ref, wl, f"{wl.name} step {i} pos {pos}")
+        assert res.nonfinite[0] == 0
+        assert int(res.ids[0]) == int(np.argmax(res.logits[0]))   # device argmax = argmax of its logits
+        strict += assert_greedy(res.ids[0], ref, f"{wl.name} step {i}")
+        if i + 1 >= n_prompt:
+            toks.append(oracle.argmax(ref))
+        pos += 1
+    if check_kv:
+        n = pos
+        for l in range(wl.n_layers):
+            for which, store in ((0, orc.K[0][l]), (1, orc.V[0][l])):
+                got = kv_as_float(read_kv(dec.kv(l, which), 0, n))
+                assert_close(got, kv_as_float(store[:n]), wl, f"{wl.name} KV layer {l} which {which}")
+    st = dec.stats()
+    dec.close()
+    return strict, st
+
+
+@pytest.mark.parametrize("name", ["tiny", "tiny_gain"])
+def test_tiny_prompt_then_greedy(name):
+    wl = gen.WORKLOADS[name]
+    strict, st = _run_sequence(wl, wl.prompt_len, wl.decode_steps)
+    assert st["replays"] == wl.prompt_len + wl.decode_steps
+    assert st["graph_nodes"] == st["kernels_per_step"]
+
+
+@pytest.mark.parametrize("kv_heads", [1, 2])
+def test_tiny_gqa_groups(kv_heads):
+    wl = gen.WORKLOADS["tiny"].replace(name=f"tiny_kv{kv_heads}", n_kv_heads=kv_heads)
+    _run_sequence(wl, 16, 8)
+
+
+def test_tiny_bf16_weights_and_kv():
+    wl = gen.WORKLOADS["tiny"].replace(name="tiny_bf16", wdtype="bf16", kvdtype="bf16")
+    _run_sequence(wl, 16, 16)
+
+
+def test_1b_prompt_then_greedy():
+    # configuration 2: 128 prompt tokens stepped in, then 256 greedy decode steps
+    wl = gen.WORKLOADS["1b"]
+    strict, st = _run_sequence(wl, wl.prompt_len, wl.decode_steps)
+    assert strict > 0
+
+
+def test_capture_equals_eager_bit_exact():
+    # "Execution", section "Verification", tier 1: capture versus eager on one device is bit-exact
+    wl = gen.WORKLOADS["1b"].replace(name="1b_l2", n_layers=2, cap=256)
+    dec, mw = make_decoder(wl)
+    toks = gen.prompt_tokens(wl, n=40)
+
+    def run():
+        out = [dec.step([t], [p]).logits[0].copy() for p, t in enumerate(toks)]
+        kv = [dec.kv(l, w).clone() for l in range(wl.n_layers) for w in (0, 1)]
+        return out, kv
+
+    graph_logits, graph_kv = run()
+    dec.reset_state()
+    dec.set_eager(True)
+    eager_logits, eager_kv = run()
+    dec.reset_state()
+    dec.set_eager(False)
+    again_logits, _ = run()
+    st = dec.stats()
+    dec.close()
+    for a, b, c in zip(graph_logits, eager_logits, again_logits):
+        assert np.array_equal(a, b)
+        assert np.array_equal(a, c)
+    import torch
+    for a, b in zip(graph_kv, eager_kv):
+        assert torch.equal(a, b)
+    assert st["eager_steps"] == len(toks)
+
+
+def test_garbage_after_pos_is_bit_identical():
+    # masked positions never reach the result ("Execution", section "A constant-shape decode graph")
+    import torch
+    wl = gen.WORKLOADS["1b"].replace(name="1b_l3", n_layers=3, cap=1024)
+    dec, mw = make_decoder(wl)
+    toks = gen.prompt_tokens(wl, n=300)
+    for p, t in enumerate(toks[:-1]):
+        dec.step([t], [p])
+    P = len(toks) - 1
+    saved = [dec.kv(l, w).clone() for l in range(wl.n_layers) for w in (0, 1)]
+    clean = dec.step([toks[-1]], [P])
+    garbage = torch.tensor([float("nan"), float("inf"), -float("inf"), 1e30], dtype=torch.bfloat16,
+                           device="cuda:0")
+    for k, (l, w) in enumerate((l, w) for l in range(wl.n_layers) for w in (0, 1)):
+        store = dec.kv(l, w)
+        store.copy_(saved[k])
+        tail = store[:, :, P + 1:, :]
+        tail.copy_(garbage.repeat(tail.numel() // 4 + 1)[: tail.numel()].view(tail.shape))
+    dirty = dec.step([toks[-1]], [P])
+    dec.close()
+    assert np.array_equal(clean.logits, dirty.logits)
+    assert np.array_equal(clean.ids, dirty.ids)
+
+
+def test_kv_write_touches_only_pos():
+    import torch
+    wl = gen.WORKLOADS["1b"].replace(name="1b_l2b", n_layers=2, cap=512)
+    dec, mw = make_decoder(wl)
+    for p, t in enumerate(gen.prompt_tokens(wl, n=10)):
+        dec.step([t], [p])
+    before = [dec.kv(l, w).clone() for l in range(2) for w in (0, 1)]
+    dec.step([5], [200])   # a later position, gap in between
+    for k, (l, w) in enumerate((l, w) for l in range(2) for w in (0, 1)):
+        changed = (dec.kv(l, w) != before[k]).any(dim=3).any(dim=1)[0]   # [cap]
+        idx = torch.nonzero(changed).flatten().tolist()
+        assert idx == [200], (l, w, idx)
+    dec.close()
+
+
+def _prefill_both(dec, orc, wl, row, npos, slot_map=None):
+    from gen.device import place_kv
+    for l in range(wl.n_layers):
+        for which in (0, 1):
+            blk = gen.kv_prefill(wl, l, which, row, npos)
+            place_kv(dec.kv(l, which), blk, row, 0, slot_map, wl.page_size)
+            store = orc.K[0][l] if which == 0 else orc.V[0][l]
+            store[:npos] = blk
+
+
+@pytest.mark.slow
+def test_8b_decode_at_prefilled_positions():
+    # configuration 3 at full size: one step at pos in {1, 1024, 4096, 8191} over KV pre-filled N(0,1)
+    wl = gen.WORKLOADS["8b"]
+    dec, mw = make_decoder(wl)
+    orc = oracle.Oracle(mw, cap=wl.cap)
+    tok = int(gen.prompt_tokens(wl, n=1)[0])
+    for pos in wl.positions:
+        dec.reset_state()
+        for l in range(wl.n_layers):
+            orc.K[0][l][:] = 0
+            orc.V[0][l][:] = 0
+        _prefill_both(dec, orc, wl, 0, pos)
+        res = dec.step([tok], [pos])
+        ref = orc.step(0, tok, pos)
+        assert_close(res.logits[0], ref, wl, f"8b pos {pos}")
+        assert_greedy(res.ids[0], ref, f"8b pos {pos}")
+        from gen.device import read_kv
+        for l in (0, wl.n_layers // 2, wl.n_layers - 1):
+            got = kv_as_float(read_kv(dec.kv(l, 0), 0, pos + 1))
+            assert_close(got[pos], kv_as_float(orc.K[0][l][pos]), wl, f"8b K write layer {l}")
+            assert np.array_equal(got[:pos], kv_as_float(orc.K[0][l][:pos]))   # prefill untouched
+    dec.close()
+
+
+@pytest.mark.slow
+def test_1b_long_cap_rows4():
+    # configuration 5: cap 32768, 4 rows at pos {100, 8000, 20000, 32767}
+    wl = gen.WORKLOADS["1b_long"]
+    dec, mw = make_decoder(wl)
+    positions = gen.row_positions(wl)
+    toks = gen.prompt_tokens(wl, n=wl.rows)
+    from gen.device import place_kv
+    for r in range(wl.rows):
+        for l in range(wl.n_layers):
+            for which in (0, 1):
+                place_kv(dec.kv(l, which), gen.kv_prefill(wl, l, which, r, int(positions[r])), r)
+    res = dec.step(toks, positions)
+    for r in range(wl.rows):
+        orc = oracle.Oracle(mw, cap=wl.cap)
+        for l in range(wl.n_layers):
+            orc.K[0][l][: positions[r]] = gen.kv_prefill(wl, l, 0, r, int(positions[r]))
+            orc.V[0][l][: positions[r]] = gen.kv_prefill(wl, l, 1, r, int(positions[r]))
+        ref = orc.step(0, int(toks[r]), int(positions[r]))
+        assert_close(res.logits[r], ref, wl, f"1b_long row {r}")
+        assert_greedy(res.ids[r], ref, f"1b_long row {r}")
+        del orc
+    dec.close()
+
+
+def _paged_case(base: str, rows: int, n_steps: int, n_layers=None):
+    """Paged KV through a seeded random page table, rows at independent positions,
+    compared with the oracle row by row; the KV write lands only at WriteMap."""
+    import torch
+    wl = gen.WORKLOADS[base]
+    kw = dict(name=f"{base}_paged{rows}", rows=rows, layout="paged", page_size=16,
+              num_pages=rows * wl.cap // 16 + 7)
+    if n_layers:
+        kw["n_layers"] = n_layers
+    wl = wl.replace(**kw)
+    dec, mw = make_decoder(wl)
+    sm = gen.permutation(wl.seed, 99, wl.num_pages)[: rows * (wl.cap // 16)].reshape(rows, wl.cap // 16)
+    dec.set_slot_map(sm)
+    orcs = [oracle.Oracle(mw, cap=wl.cap) for _ in range(rows)]
+    start = [int(x) for x in gen.ints(wl.seed, 98, 0, wl.cap - n_steps, rows)]
+    toks = [gen.prompt_tokens(wl, row=r, n=n_steps) for r in range(rows)]
+    for i in range(n_steps):
+        pos = [start[r] + i for r in range(rows)]
+        before = [dec.kv(l, 0).clone() for l in range(wl.n_layers)]
+        res = dec.step([toks[r][i] for r in range(rows)], pos)
+        wmap = [int(sm[r][p // 16]) * 16 + p % 16 for r, p in enumerate(pos)]
+        for l in range(wl.n_layers):
+            diff = (dec.kv(l, 0) != before[l]).any(dim=3).any(dim=1)   # [pages, page]
+            got = sorted((int(a) * 16 + int(b)) for a, b in torch.nonzero(diff).tolist())
+            assert got == sorted(wmap), (l, got, wmap)
+        for r in range(rows):
+            # the oracle sees only positions the step wrote: zeros before start (same as the GPU pool)
+            ref = orcs[r].step(0, int(toks[r][i]), pos[r])
+            assert_close(res.logits[r], ref, wl, f"{wl.name} row {r} step {i}")
+            assert_greedy(res.ids[r], ref)
+    dec.close()
+
+
+def test_paged_tiny_rows2():
+    _paged_case("tiny", 2, 12)
+
+
+def test_paged_1b_rows4():
+    _paged_case("1b", 4, 6, n_layers=4)
