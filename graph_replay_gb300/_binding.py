@@ -80,6 +80,8 @@ _SIG = [
     ("dec_stream", ctypes.c_int, [_P, ctypes.POINTER(_P)]),
     ("dec_stats_get", ctypes.c_int, [_P, ctypes.POINTER(dec_stats)]),
     ("dec_launch_kernel", ctypes.c_int, [_P, _I32, _I32, ctypes.POINTER(_I64)]),
+    ("dec_trace", ctypes.c_int, [_P, _I32]),
+    ("dec_trace_read", ctypes.c_int, [_P, _P, ctypes.c_size_t]),
     ("dec_debug_busy", ctypes.c_int, [_P, _I64]),
     ("dec_set_timeout", ctypes.c_int, [_P, _I64]),
     ("dec_last_error", ctypes.c_char_p, [_P]),
@@ -217,6 +219,17 @@ def dec_launch_kernel(h, index: int, pdl: bool = False) -> int:
     n = ctypes.c_int64()
     check(h, lib().dec_launch_kernel(h, index, 1 if pdl else 0, ctypes.byref(n)))
     return n.value
+
+
+def dec_trace(h, enable: bool) -> None:
+    check(h, lib().dec_trace(h, 1 if enable else 0))
+
+
+def dec_trace_read(h, n_kernels: int):
+    import numpy as np
+    out = np.zeros(4 * n_kernels, dtype=np.uint64)
+    check(h, lib().dec_trace_read(h, out.ctypes.data, n_kernels))
+    return out.reshape(n_kernels, 4)
 
 
 def dec_debug_busy(h, microseconds: int) -> None:

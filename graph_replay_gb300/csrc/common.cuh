@@ -11,6 +11,7 @@ constexpr unsigned FAULT_TOKEN = 0x1u;
 constexpr unsigned FAULT_POS = 0x2u;
 constexpr unsigned FAULT_WRITE_MAP = 0x4u;
 constexpr unsigned FAULT_SLOT_MAP = 0x8u;
+constexpr unsigned FAULT_WAIT = 0x10u;   // an in-kernel wait gave up (bounded spin)
 
 // ---- programmatic dependent launch (griddepcontrol) ----
 // wait: block until the preceding kernel in the stream/graph has completed and
@@ -18,6 +19,24 @@ constexpr unsigned FAULT_SLOT_MAP = 0x8u;
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 // trigger: allow the dependent kernel to start launching its CTAs.
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ---- in-graph trace (profiling) ----
+// A trace buffer holds an enable word followed by 4 stamps per recorded
+// kernel: [earliest CTA entry, latest CTA past the dependency wait, earliest
+// CTA exit, latest CTA exit], in %globaltimer nanoseconds.
+__device__ __forceinline__ unsigned long long gtimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void trace_stamp(unsigned long long* tr, int id, int slot) {
+    if (tr && *reinterpret_cast<volatile unsigned long long*>(tr)) {
+        unsigned long long* w = tr + 1 + 4 * id + slot;
+        const unsigned long long t = gtimer();
+        if (slot == 0 || slot == 2) atomicMin(w, t);
+        else atomicMax(w, t);
+    }
+}
 
 // ---- loads ----
 // 16-byte streaming load of data read once per step (weights, KV): read-only
@@ -33,6 +52,51 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
 // bulk prefetch of [p, p + bytes) into L2 (p and bytes multiples of 16)
 __device__ __forceinline__ void prefetch_l2_bulk(const void* p, unsigned bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// ---- shared-memory barriers and bulk copies (TMA engine, no tensor map) ----
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+// make barrier initialisation visible to the async (bulk-copy) proxy
+__device__ __forceinline__ void mbar_fence_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait for the phase with the given parity to complete: false after
+// MBAR_POLLS polls (each poll may suspend briefly), never an endless spin.
+constexpr uint32_t MBAR_POLLS = 1u << 22;
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    for (uint32_t i = 0; i < MBAR_POLLS; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+// global -> shared bulk copy completing on an mbarrier (16-byte aligned
+// addresses, size a multiple of 16)
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+// named barrier over `threads` threads (a multiple of 32)
+__device__ __forceinline__ void named_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 // ---- bf16 unpacking (exact widening) ----

@@ -49,8 +49,11 @@ int es_of(int dtype) { return dtype == DEC_DTYPE_BF16 ? 2 : 4; }
 
 // Offsets of every buffer of a capture inside one workspace.
 struct WsLayout {
-    size_t status, slots, slot_map, counters, x, qkv, attn, gu, logits, part, rope, kv, kv_layer, total;
+    size_t status, slots, slot_map, counters, trace, x, qkv, attn, gu, logits, part, rope, kv, kv_layer, total;
 };
+
+// kernels recorded per step: embedding, 5 per layer, head
+int kernels_per_step(int n_layers) { return 2 + 5 * n_layers; }
 
 bool compute_layout(const dec_config& c, int cap, int R, int layout, int page, int npages, WsLayout* L) {
     const size_t hd = (size_t)c.head_dim, Hq = (size_t)c.n_heads, Hkv = (size_t)c.n_kv_heads;
@@ -62,6 +65,7 @@ bool compute_layout(const dec_config& c, int cap, int R, int layout, int page, i
     L->slots = take(3 * (size_t)R * sizeof(int32_t));
     L->slot_map = take(layout == DEC_KV_PAGED ? (size_t)R * (cap / page) * sizeof(int32_t) : 0);
     L->counters = take((size_t)R * Hkv * sizeof(unsigned));
+    L->trace = take((1 + 4 * (size_t)kernels_per_step(c.n_layers)) * sizeof(unsigned long long));
     L->x = take((size_t)R * d * 4);
     L->qkv = take((size_t)R * (Hq + 2 * Hkv) * hd * 4);
     L->attn = take((size_t)R * Hq * hd * 4);
@@ -109,6 +113,7 @@ struct dec_handle {
     int32_t* d_slots = nullptr;
     int32_t* d_slot_map = nullptr;
     unsigned* d_counters = nullptr;
+    unsigned long long* d_trace = nullptr;
     float *d_x = nullptr, *d_qkv = nullptr, *d_attn = nullptr, *d_gu = nullptr, *d_logits = nullptr;
     float* d_part = nullptr;
     float2* d_rope = nullptr;
@@ -253,13 +258,17 @@ std::vector<float2> rope_table(int cap, int hd, double theta) {
     return t;
 }
 
+cudaError_t launch_attn(const AttnPlan& a, cudaStream_t s, bool pdl) {
+    return a.mma ? attn_mma_launch(a, s, pdl) : attn_launch(a, s, pdl);
+}
+
 // launch the whole step (the sequence the graph records)
 cudaError_t enqueue_step(dec_handle* h) {
     cudaError_t e = embed_launch(h->cfg.weight_dtype == DEC_DTYPE_BF16 ? W_BF16 : W_F32, h->embed_p, h->stream);
     if (e != cudaSuccess) return e;
     for (int l = 0; l < h->cfg.n_layers; ++l) {
         if ((e = gemv_launch(h->gemv[4 * l + 0], h->stream, h->pdl)) != cudaSuccess) return e;
-        if ((e = attn_launch(h->attn[l], h->stream, h->pdl)) != cudaSuccess) return e;
+        if ((e = launch_attn(h->attn[l], h->stream, h->pdl)) != cudaSuccess) return e;
         if ((e = gemv_launch(h->gemv[4 * l + 1], h->stream, h->pdl)) != cudaSuccess) return e;
         if ((e = gemv_launch(h->gemv[4 * l + 2], h->stream, h->pdl)) != cudaSuccess) return e;
         if ((e = gemv_launch(h->gemv[4 * l + 3], h->stream, h->pdl)) != cudaSuccess) return e;
@@ -461,6 +470,7 @@ int dec_capture(dec_handle* h, int32_t cap, int32_t rows, int32_t kv_layout, int
     h->d_slots = (int32_t*)(h->ws + L.slots);
     h->d_slot_map = kv_layout == DEC_KV_PAGED ? (int32_t*)(h->ws + L.slot_map) : nullptr;
     h->d_counters = (unsigned*)(h->ws + L.counters);
+    h->d_trace = (unsigned long long*)(h->ws + L.trace);
     h->d_x = (float*)(h->ws + L.x);
     h->d_qkv = (float*)(h->ws + L.qkv);
     h->d_attn = (float*)(h->ws + L.attn);
@@ -502,7 +512,7 @@ int dec_capture(dec_handle* h, int32_t cap, int32_t rows, int32_t kv_layout, int
     const int hd = c.head_dim, Hq = c.n_heads, Hkv = c.n_kv_heads, d = c.d_model, F = c.ffn_hidden;
     const int qkv_stride = (Hq + 2 * Hkv) * hd;
     h->embed_p = EmbedParams{h->embed, h->d_slots, h->d_slots + rows, rows, c.vocab, d, cap, h->d_x,
-                             &h->d_status->err, h->d_status->amax, h->d_status->nonfinite};
+                             &h->d_status->err, h->d_status->amax, h->d_status->nonfinite, h->d_trace, 0};
     h->gemv.clear();
     h->attn.clear();
     auto mk = [&](int pro, int epi, const void* w0, int n0, const void* w1, int n1, const void* w2, int n2, int K,
@@ -525,6 +535,8 @@ int dec_capture(dec_handle* h, int32_t cap, int32_t rows, int32_t kv_layout, int
         p.out_stride = out_stride;
         p.amax = h->d_status->amax;
         p.nonfinite = h->d_status->nonfinite;
+        p.err = &h->d_status->err;
+        p.trace = h->d_trace;
         return pl;
     };
     for (int l = 0; l < c.n_layers; ++l) {
@@ -560,21 +572,40 @@ int dec_capture(dec_handle* h, int32_t cap, int32_t rows, int32_t kv_layout, int
         p.out = h->d_attn;
         p.err = &h->d_status->err;
         p.scale = (float)(1.0 / std::sqrt((double)hd));
+        p.trace = h->d_trace;
+        p.trace_id = 2 + 5 * l;
         h->attn.push_back(ap);
     }
     h->gemv.push_back(mk(PRO_RMSNORM, EPI_LOGITS, h->lm_head, c.vocab, nullptr, 0, nullptr, 0, d, h->d_x, d,
                          h->final_norm, h->d_logits, c.vocab));
+    for (int l = 0; l < c.n_layers; ++l) {
+        h->gemv[4 * l + 0].p.trace_id = 1 + 5 * l;
+        h->gemv[4 * l + 1].p.trace_id = 3 + 5 * l;
+        h->gemv[4 * l + 2].p.trace_id = 4 + 5 * l;
+        h->gemv[4 * l + 3].p.trace_id = 5 + 5 * l;
+    }
+    h->gemv.back().p.trace_id = 5 * c.n_layers + 1;
     for (auto& pl : h->gemv) {
         if ((e = gemv_plan(&pl, h->num_sms)) != cudaSuccess)
             return fail(h, DEC_E_UNSUPPORTED, "no GEMV kernel for rows=%d K=%d N=%d (%s)", rows, pl.p.K, pl.p.N,
                         cudaGetErrorString(e));
     }
+    const char* att_env = getenv("GRAPHDEC_ATTN");   // "simd" selects the CUDA-core attention kernel
+    const bool allow_mma = !(att_env && strcmp(att_env, "simd") == 0);
     for (auto& ap : h->attn) {
+        if (allow_mma && attn_mma_supported(ap.kvtype, hd, Hq / Hkv, ap.paged, ap.p.page_size)) {
+            if ((e = attn_mma_plan(&ap, h->num_sms)) != cudaSuccess)
+                return fail(h, DEC_E_UNSUPPORTED, "no attention kernel for head_dim=%d group=%d cap=%d (%s)", hd,
+                            Hq / Hkv, cap, cudaGetErrorString(e));
+            continue;
+        }
         if ((e = attn_plan(&ap, h->num_sms)) != cudaSuccess)
             return fail(h, DEC_E_UNSUPPORTED, "no attention kernel for head_dim=%d group=%d cap=%d (%s)", hd,
                         Hq / Hkv, cap, cudaGetErrorString(e));
     }
-    h->kernels = 2 + 5 * c.n_layers;
+    h->kernels = kernels_per_step(c.n_layers);
+    if ((e = cudaMemsetAsync(h->d_trace, 0, sizeof(unsigned long long), h->stream)) != cudaSuccess)
+        return cuda_fail(h, e, "trace clear");
 
     // ---- one eager step (launch checks), then a clean state ----
     if ((e = zero_state(h)) != cudaSuccess) return cuda_fail(h, e, "state clear");
@@ -770,7 +801,7 @@ int dec_launch_kernel(dec_handle* h, int32_t index, int32_t pdl, int64_t* bytes)
         const int l = (index - 1) / 5, k = (index - 1) % 5;
         if (k == 1) {
             const AttnPlan& a = h->attn[l];
-            e = attn_launch(a, h->stream, pdl != 0);
+            e = launch_attn(a, h->stream, pdl != 0);
             b = R * 2 * (int64_t)h->cap * c.n_kv_heads * c.head_dim * kes +
                 R * (int64_t)(c.n_heads + 2 * c.n_kv_heads) * c.head_dim * 4 + R * (int64_t)c.n_heads * c.head_dim * 4;
         } else {
@@ -784,6 +815,32 @@ int dec_launch_kernel(dec_handle* h, int32_t index, int32_t pdl, int64_t* bytes)
     }
     if (e != cudaSuccess) return cuda_fail(h, e, "kernel launch");
     if (bytes) *bytes = b;
+    return DEC_OK;
+}
+
+int dec_trace(dec_handle* h, int32_t enable) {
+    int rc = gate(h, true);
+    if (rc) return rc;
+    if ((rc = bounded_wait(h)) != DEC_OK) return rc;
+    const size_t n = 1 + 4 * (size_t)h->kernels;
+    std::vector<unsigned long long> init(n, 0ull);
+    init[0] = enable ? 1ull : 0ull;
+    for (int k = 0; k < h->kernels; ++k) {
+        init[1 + 4 * k + 0] = ~0ull;   // minima start high
+        init[1 + 4 * k + 2] = ~0ull;
+    }
+    cudaError_t e = cudaMemcpy(h->d_trace, init.data(), n * sizeof(unsigned long long), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(h, e, "trace reset");
+    return DEC_OK;
+}
+
+int dec_trace_read(dec_handle* h, uint64_t* out, size_t n_kernels) {
+    int rc = gate(h, true);
+    if (rc) return rc;
+    if (!out || n_kernels > (size_t)h->kernels) return fail(h, DEC_E_INVALID, "dec_trace_read: bad buffer");
+    if ((rc = bounded_wait(h)) != DEC_OK) return rc;
+    cudaError_t e = cudaMemcpy(out, h->d_trace + 1, 4 * n_kernels * sizeof(unsigned long long), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(h, e, "trace read");
     return DEC_OK;
 }
 
@@ -841,6 +898,7 @@ int dec_destroy(dec_handle* h) {
         if (h->own_stream && h->stream) cudaStreamDestroy(h->stream);
     }
     // a poisoned handle leaks what the pending work could reference
+    for (auto& a : h->attn) attn_mma_release(a);
     delete h;
     return DEC_OK;
 }

@@ -48,17 +48,21 @@ struct GemvParams {
     int out_stride;
     unsigned long long* amax;  // [R] argmax keys (EPI_LOGITS)
     unsigned* nonfinite;       // [R] flags (EPI_LOGITS)
-    int rows_per_cta;
+    unsigned* err;             // error word (FAULT_WAIT)
+    int rps;                   // weight rows per ring stage
+    int stages;                // ring stages
+    unsigned long long* trace; // trace buffer or null
+    int trace_id;
 };
 
 struct GemvPlan {
-    int wtype, pro, epi, nr;
+    int wtype, pro, epi, nr, cpl;
     int grid, block;
     size_t smem;
     GemvParams p;
 };
 
-// Fill plan->grid/block/smem/nr and p.rows_per_cta for the given shape.
+// Fill plan->grid/block/smem/nr/cpl and p.rps/p.stages for the given shape.
 cudaError_t gemv_plan(GemvPlan* plan, int num_sms);
 cudaError_t gemv_launch(const GemvPlan& plan, cudaStream_t s, bool pdl);
 
@@ -74,12 +78,15 @@ struct AttnParams {
     const float2* rope;    // [cap, hd/2] (cos, sin)
     int cap, R, Hq, Hkv, hd;
     int split_len, nsplit;
+    int stages;            // ring stages
     int page_size, pages_per_row, num_pages;
     float* part;           // [R, Hq, nsplit, hd + 2] partial (m, l, o)
     unsigned* counters;    // [R, Hkv] split-completion counters (zero between steps)
     float* out;            // [R, Hq * hd]
     unsigned* err;
     float scale;
+    unsigned long long* trace;
+    int trace_id;
 };
 
 struct AttnPlan {
@@ -90,12 +97,20 @@ struct AttnPlan {
     int block;
     size_t smem;
     AttnParams p;
+    bool mma = false;              // tensor-core kernel (attn_mma.cu)
+    void* mma_params = nullptr;    // its parameter block (tensor maps + p), owned by the plan
 };
 
 // choose split_len / nsplit; returns cudaErrorInvalidValue for unsupported head_dim / group
 cudaError_t attn_plan(AttnPlan* plan, int num_sms);
 cudaError_t attn_launch(const AttnPlan& plan, cudaStream_t s, bool pdl);
 size_t attn_part_floats(int R, int Hq, int hd, int nsplit);
+
+// tensor-core variant for bf16 K/V (head_dim 64 or 128)
+bool attn_mma_supported(int kvtype, int hd, int G, bool paged, int page_size);
+cudaError_t attn_mma_plan(AttnPlan* plan, int num_sms);
+cudaError_t attn_mma_launch(const AttnPlan& plan, cudaStream_t s, bool pdl);
+void attn_mma_release(AttnPlan& plan);
 
 // ---------------- embedding gather + per-step resets ----------------
 struct EmbedParams {
@@ -107,6 +122,8 @@ struct EmbedParams {
     unsigned* err;
     unsigned long long* amax;
     unsigned* nonfinite;
+    unsigned long long* trace;
+    int trace_id;
 };
 cudaError_t embed_launch(int wtype, const EmbedParams& p, cudaStream_t s);
 

@@ -16,6 +16,7 @@ namespace gd {
 template <typename WT>
 __global__ void __launch_bounds__(256) k_embed(const EmbedParams p) {
     const int tid = threadIdx.x;
+    if (tid == 0) trace_stamp(p.trace, p.trace_id, 0);
     if (tid == 0) *p.err = 0u;
     if (tid < p.R) {
         p.amax[tid] = 0ull;
@@ -33,7 +34,21 @@ __global__ void __launch_bounds__(256) k_embed(const EmbedParams p) {
         if ((pos < 0 || pos >= p.cap) && tid == 0) atomicOr(p.err, FAULT_POS);
         const WT* e = E + (size_t)tok * p.d;
         float* x = p.x + (size_t)r * p.d;
-        for (int i = tid; i < p.d; i += blockDim.x) x[i] = Elem<WT>::load1(e + i);
+        // 16-byte loads, all in flight at once (d is a multiple of the vector width)
+        constexpr int VEC = Elem<WT>::VEC;
+        for (int i = tid * VEC; i < p.d; i += blockDim.x * VEC) {
+            float f[VEC];
+            Elem<WT>::unpack(*reinterpret_cast<const uint4*>(e + i), f);
+#pragma unroll
+            for (int q = 0; q < VEC; q += 4)
+                *reinterpret_cast<float4*>(x + i + q) = make_float4(f[q], f[q + 1], f[q + 2], f[q + 3]);
+        }
+    }
+    __syncthreads();
+    if (tid == 0) {
+        trace_stamp(p.trace, p.trace_id, 1);
+        trace_stamp(p.trace, p.trace_id, 2);
+        trace_stamp(p.trace, p.trace_id, 3);
     }
 }
 

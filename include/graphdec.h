@@ -248,6 +248,17 @@ int dec_stats_get(const dec_handle *h, dec_stats *out);
  * cap-swept K/V + q + partials for attention). */
 int dec_launch_kernel(dec_handle *h, int32_t index, int32_t pdl, int64_t *bytes);
 
+/* In-graph trace (profiling).  enable = 1 clears the stamps and makes every
+ * recorded kernel stamp the device's global nanosecond timer at: its earliest
+ * CTA entry, the latest CTA to pass the wait on the previous kernel, its
+ * earliest CTA exit and its latest CTA exit; enable = 0 stops recording.
+ * Stamps accumulate (min / max) over the steps run while enabled. */
+int dec_trace(dec_handle *h, int32_t enable);
+
+/* Copy 4 stamps per kernel for the first n_kernels kernels of the step
+ * (order as in dec_launch_kernel) into out[4 * n_kernels] (host). */
+int dec_trace_read(dec_handle *h, uint64_t *out, size_t n_kernels);
+
 /* Test hook for the bounded wait: enqueue a kernel that busies one SM for
  * about `microseconds` (clamped to [0, 2000000]) and then ends by itself. */
 int dec_debug_busy(dec_handle *h, int64_t microseconds);

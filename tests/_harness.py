@@ -55,6 +55,26 @@ def assert_close(gpu, ref, wl, what=""):
     return max_abs, rel_l2
 
 
+def assert_close_state(gpu, ref, wl, what=""):
+    """Carried K/V state.  Stored values are rounded to the KV dtype, and the GPU
+    rounds an fp32 value where the oracle rounds the exact one, so a value near a
+    rounding midpoint may land one storage ulp away: each element may differ by
+    max(logit max-abs bound, one bf16 ulp = 2^-7 |ref| at most); relative L2 as
+    for logits.  fp32 stores keep the fp32 bound."""
+    gpu = np.asarray(gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    bad = np.isfinite(ref) & ~np.isfinite(gpu)
+    assert not bad.any(), f"{what}: non-finite GPU values where the oracle is finite"
+    if wl.kvdtype == "f32" and wl.wdtype == "f32":
+        return assert_close(gpu, ref, wl, what)
+    d = np.abs(gpu - ref)
+    bound = np.maximum(BF16_MAX_ABS, np.abs(ref) * 2.0 ** -7)
+    worst = float((d / bound).max())
+    _, rel_l2, _ = errors(gpu, ref)
+    assert worst <= 1.0 and rel_l2 <= BF16_REL_L2, f"{what}: worst |d|/bound {worst:.3f}, rel L2 {rel_l2:.3e}"
+    return worst, rel_l2
+
+
 def assert_greedy(gpu_id, ref_logits, what=""):
     """Bit-exact id wherever the oracle's top-2 margin exceeds 0.05; otherwise the
     GPU id must be one of the oracle's near-top candidates."""

@@ -11,7 +11,7 @@ import pytest
 
 import gen
 import oracle
-from _harness import assert_close, assert_greedy, kv_as_float, make_decoder
+from _harness import assert_close, assert_close_state, assert_greedy, kv_as_float, make_decoder
 
 pytestmark = pytest.mark.gpu
 
@@ -40,7 +40,7 @@ def _run_sequence(wl, n_prompt, n_decode, mw=None, check_kv=True, rows=None):
         for l in range(wl.n_layers):
             for which, store in ((0, orc.K[0][l]), (1, orc.V[0][l])):
                 got = kv_as_float(read_kv(dec.kv(l, which), 0, n))
-                assert_close(got, kv_as_float(store[:n]), wl, f"{wl.name} KV layer {l} which {which}")
+                assert_close_state(got, kv_as_float(store[:n]), wl, f"{wl.name} KV layer {l} which {which}")
     st = dec.stats()
     dec.close()
     return strict, st
@@ -170,7 +170,7 @@ def test_8b_decode_at_prefilled_positions():
         from gen.device import read_kv
         for l in (0, wl.n_layers // 2, wl.n_layers - 1):
             got = kv_as_float(read_kv(dec.kv(l, 0), 0, pos + 1))
-            assert_close(got[pos], kv_as_float(orc.K[0][l][pos]), wl, f"8b K write layer {l}")
+            assert_close_state(got[pos], kv_as_float(orc.K[0][l][pos]), wl, f"8b K write layer {l}")
             assert np.array_equal(got[:pos], kv_as_float(orc.K[0][l][:pos]))   # prefill untouched
     dec.close()
 
