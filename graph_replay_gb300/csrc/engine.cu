@@ -844,6 +844,51 @@ int dec_trace_read(dec_handle* h, uint64_t* out, size_t n_kernels) {
     return DEC_OK;
 }
 
+}  // extern "C"
+
+namespace gd {
+
+// One layer's attention on caller buffers: the recorded plan with its q/k/v
+// input, position slot, output and split scratch replaced.  Synchronous.
+int engine_run_attention(dec_handle* h, int32_t layer, const float* qkv, const int32_t* pos, float* out, float* part,
+                         unsigned* counters) {
+    if (layer < 0 || layer >= h->cfg.n_layers) return fail(h, DEC_E_INVALID, "layer %d out of range", layer);
+    if (!qkv || !pos || !out) return fail(h, DEC_E_INVALID, "qkv, pos and out are required");
+    if (h->state == ST_NEEDS_RESET) return fail(h, DEC_E_NEEDS_RESET, "an earlier step failed; call dec_reset_state");
+    AttnPlan a = h->attn[layer];
+    a.p.qkv = qkv;
+    a.p.qkv_stride = (h->cfg.n_heads + 2 * h->cfg.n_kv_heads) * h->cfg.head_dim;
+    a.p.pos = pos;
+    a.p.out = out;
+    a.p.part = part;
+    a.p.counters = counters;
+    a.p.trace = nullptr;
+    cudaError_t e = cudaMemsetAsync(&h->d_status->err, 0, sizeof(unsigned), h->stream);
+    if (e == cudaSuccess) e = launch_attn(a, h->stream, false);
+    if (e != cudaSuccess) return cuda_fail(h, e, "attention launch");
+    if ((e = cudaMemcpyAsync(&h->h_status->err, &h->d_status->err, sizeof(unsigned), cudaMemcpyDeviceToHost,
+                             h->stream)) != cudaSuccess)
+        return cuda_fail(h, e, "status readback");
+    int rc = bounded_wait(h);
+    if (rc != DEC_OK) return rc;
+    if (h->h_status->err) {
+        h->last_fault = h->h_status->err;
+        h->state = ST_NEEDS_RESET;
+        return fail(h, DEC_E_DEVICE_FAULT, "device check failed (error word 0x%x)", h->h_status->err);
+    }
+    return DEC_OK;
+}
+
+}  // namespace gd
+
+extern "C" {
+
+int dec_attention(dec_handle* h, int32_t layer, const float* qkv, const int32_t* pos, float* out) {
+    int rc = gate(h, true);
+    if (rc) return rc;
+    return engine_run_attention(h, layer, qkv, pos, out, h->d_part, h->d_counters);
+}
+
 int dec_debug_busy(dec_handle* h, int64_t microseconds) {
     int rc = gate(h, true);
     if (rc) return rc;

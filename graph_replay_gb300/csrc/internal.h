@@ -131,3 +131,12 @@ cudaError_t embed_launch(int wtype, const EmbedParams& p, cudaStream_t s);
 cudaError_t busy_launch(long long ns, cudaStream_t s);
 
 }  // namespace gd
+
+struct dec_handle;
+namespace gd {
+// engine services for other translation units of the library
+int engine_run_attention(dec_handle* h, int32_t layer, const float* qkv, const int32_t* pos, float* out, float* part,
+                         unsigned* counters);
+
+
+}  // namespace gd

@@ -76,6 +76,9 @@ class Decoder:
             self.h = None
             raise
         self.vocab = cfg.vocab
+        self.device = torch.device(f"cuda:{cfg.device}")
+        self._hstream = torch.cuda.ExternalStream(B.dec_stream(self.h), device=self.device)
+        self._ev = torch.cuda.Event()
         self._logits = np.empty((rows, cfg.vocab), dtype=np.float32)
         self._ids = np.empty(rows, dtype=np.int32)
         self._nf = np.empty(rows, dtype=np.uint8)
@@ -98,11 +101,18 @@ class Decoder:
                 add(role, l, lw[name])
         return out
 
+    def _after_torch(self) -> None:
+        """Order the handle's stream after work torch queued on its current stream
+        (e.g. KV pre-fill or input tensors written through torch)."""
+        self._ev.record(torch.cuda.current_stream(self.device))
+        self._hstream.wait_event(self._ev)
+
     # ---- stepping ----
     def step(self, tokens, pos, write_map=None, logits: bool = True) -> StepResult:
         tok = np.ascontiguousarray(tokens, dtype=np.int32).reshape(self.rows)
         ps = np.ascontiguousarray(pos, dtype=np.int32).reshape(self.rows)
         wm = None if write_map is None else np.ascontiguousarray(write_map, dtype=np.int32).reshape(self.rows)
+        self._after_torch()
         rc = B.dec_step(self.h, _ptr(tok), _ptr(ps), _ptr(wm), _ptr(self._logits) if logits else None,
                         _ptr(self._ids), _ptr(self._nf))
         B.check(self.h, rc)
@@ -110,12 +120,22 @@ class Decoder:
 
     def launch(self, dev_slots: Optional[torch.Tensor]) -> None:
         """Asynchronous step from a device slot record [3*rows] int32 (tokens, pos, write map)."""
+        self._after_torch()
         B.check(self.h, B.dec_launch(self.h, None if dev_slots is None else dev_slots.data_ptr()))
 
     def wait(self, logits: bool = False) -> StepResult:
         rc = B.dec_wait(self.h, _ptr(self._logits) if logits else None, _ptr(self._ids), _ptr(self._nf))
         B.check(self.h, rc)
         return StepResult(self._logits.copy() if logits else None, self._ids.copy(), self._nf.copy())
+
+    def attention(self, layer: int, qkv: torch.Tensor, pos: torch.Tensor, out: torch.Tensor) -> None:
+        """One layer's attention on device tensors: qkv [rows, (Hq+2Hkv)*hd] fp32,
+        pos [rows] int32, out [rows, Hq*hd] fp32 (written)."""
+        for t, dt in ((qkv, torch.float32), (pos, torch.int32), (out, torch.float32)):
+            if not t.is_cuda or not t.is_contiguous() or t.dtype != dt:
+                raise ValueError("attention: contiguous CUDA tensors of the documented dtypes")
+        self._after_torch()
+        B.check(self.h, B.dec_attention(self.h, layer, qkv.data_ptr(), pos.data_ptr(), out.data_ptr()))
 
     def set_slot_map(self, slot_map: np.ndarray) -> None:
         m = np.ascontiguousarray(slot_map, dtype=np.int32)
@@ -125,6 +145,7 @@ class Decoder:
         B.dec_set_eager(self.h, eager)
 
     def reset_state(self) -> None:
+        self._after_torch()
         B.check(self.h, B.dec_reset_state(self.h))
 
     # ---- views of device state ----
@@ -147,7 +168,7 @@ class Decoder:
         return torch.as_tensor(_DevArray(ptr, (self.rows, self.vocab), "<f4"), device=f"cuda:{self.cfg.device}")
 
     def stream(self) -> torch.cuda.ExternalStream:
-        return torch.cuda.ExternalStream(B.dec_stream(self.h), device=f"cuda:{self.cfg.device}")
+        return self._hstream
 
     def stats(self) -> dict:
         st = B.dec_stats_get(self.h)

@@ -228,6 +228,21 @@ int dec_reset_state(dec_handle *h);
  * or inspect the carried state. */
 int dec_kv_ptr(dec_handle *h, int32_t layer, int32_t which, void **ptr, size_t *bytes);
 
+/* One layer's decode attention as a standalone operation, on the caller's
+ * buffers ("Execution", section "A constant-shape decode graph"): rotates q and
+ * k by RoPE at pos[r], writes the rotated k and v (rounded to the KV dtype)
+ * into this layer's KV store at pos[r] (paged: at the slot of the current
+ * write map), and attends over the full capacity with positions after pos[r]
+ * masked.  Runs on the handle's stream and waits (bounded).
+ *   layer  0 .. n_layers-1
+ *   qkv    device fp32 [rows, (n_heads + 2 * n_kv_heads) * head_dim]: q, then k,
+ *          then v of every row, before RoPE
+ *   pos    device int32 [rows], each in [0, cap)
+ *   out    device fp32 [rows, n_heads * head_dim]
+ * The split partials use the handle's workspace.  DEC_E_DEVICE_FAULT if a
+ * device check fails (the handle then needs dec_reset_state). */
+int dec_attention(dec_handle *h, int32_t layer, const float *qkv, const int32_t *pos, float *out);
+
 /* Device address of the logits [rows, vocab] fp32 of the last step. */
 int dec_logits_ptr(dec_handle *h, float **ptr);
 

@@ -239,3 +239,43 @@ def test_paged_tiny_rows2():
 
 def test_paged_1b_rows4():
     _paged_case("1b", 4, 6, n_layers=4)
+
+
+@pytest.mark.parametrize("name, rows", [("1b", 2), ("8b", 1)])
+def test_attention_op_against_oracle(name, rows):
+    """dec_attention alone: RoPE, K/V write at pos, masked full-capacity sweep,
+    against the oracle's rotation, storage rounding and causal attention."""
+    import torch
+    base = gen.WORKLOADS[name]
+    wl = base.replace(name=f"{name}_attn", n_layers=2, vocab=1024, cap=2048, rows=rows)
+    dec, mw = make_decoder(wl)
+    from gen.device import place_kv, read_kv
+    positions = [1500, 777][:rows]
+    for r in range(rows):
+        for which in (0, 1):
+            place_kv(dec.kv(1, which), gen.kv_prefill(wl, 1, which, r, positions[r]), r)
+    qkv_h = gen.normal(wl.seed, 77, (rows, wl.q_dim + 2 * wl.kv_dim), sigma=1.0, dtype="f32")
+    qkv = torch.from_numpy(qkv_h).cuda()
+    pos = torch.tensor(positions, dtype=torch.int32, device="cuda:0")
+    out = torch.empty(rows, wl.q_dim, dtype=torch.float32, device="cuda:0")
+    dec.attention(1, qkv, pos, out)
+    got = out.cpu().numpy()
+    hd, G = wl.head_dim, wl.n_heads // wl.n_kv_heads
+    for r in range(rows):
+        p = positions[r]
+        K = gen.kv_prefill(wl, 1, 0, r, p + 1).copy()
+        V = gen.kv_prefill(wl, 1, 1, r, p + 1).copy()
+        q = qkv_h[r, : wl.q_dim].astype(np.float64).reshape(wl.n_heads, hd)
+        k = qkv_h[r, wl.q_dim: wl.q_dim + wl.kv_dim].astype(np.float64).reshape(wl.n_kv_heads, hd)
+        v = qkv_h[r, wl.q_dim + wl.kv_dim:].astype(np.float64).reshape(wl.n_kv_heads, hd)
+        for gi in range(wl.n_kv_heads):
+            kr = oracle.rope(k[gi], p, wl.rope_theta)
+            K[p, gi] = [oracle.bf16_round(z) for z in kr]
+            V[p, gi] = [oracle.bf16_round(z) for z in v[gi]]
+        # the store now holds the oracle's rounding of the new k, v at p (one storage ulp allowed)
+        got_k = kv_as_float(read_kv(dec.kv(1, 0), r, p + 1))
+        assert_close_state(got_k[p], kv_as_float(K[p]), wl, "attention op K write")
+        ref = np.concatenate([oracle.attend(oracle.rope(q[i], p, wl.rope_theta), K[:, i // G], V[:, i // G])
+                              for i in range(wl.n_heads)])
+        assert_close(got[r], ref, wl, f"attention op row {r}")
+    dec.close()
