@@ -77,6 +77,7 @@ _SIG = [
     ("dec_reset_state", ctypes.c_int, [_P]),
     ("dec_kv_ptr", ctypes.c_int, [_P, _I32, _I32, ctypes.POINTER(_P), ctypes.POINTER(ctypes.c_size_t)]),
     ("dec_attention", ctypes.c_int, [_P, _I32, _P, _P, _P]),
+    ("dec_attention_static", ctypes.c_int, [_P, _I32, _P, _P, _P]),
     ("dec_logits_ptr", ctypes.c_int, [_P, ctypes.POINTER(_P)]),
     ("dec_stream", ctypes.c_int, [_P, ctypes.POINTER(_P)]),
     ("dec_stats_get", ctypes.c_int, [_P, ctypes.POINTER(dec_stats)]),
@@ -200,6 +201,10 @@ def dec_kv_ptr(h, layer, which):
 
 def dec_attention(h, layer: int, qkv_ptr, pos_ptr, out_ptr) -> int:
     return lib().dec_attention(h, layer, qkv_ptr, pos_ptr, out_ptr)
+
+
+def dec_attention_static(h, layer: int, qkv_ptr, pos_ptr, out_ptr) -> int:
+    return lib().dec_attention_static(h, layer, qkv_ptr, pos_ptr, out_ptr)
 
 
 def dec_logits_ptr(h) -> int:

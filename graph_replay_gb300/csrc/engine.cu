@@ -879,6 +879,16 @@ int engine_run_attention(dec_handle* h, int32_t layer, const float* qkv, const i
     return DEC_OK;
 }
 
+// split scratch one layer's attention needs: partial floats and counters
+void engine_attention_scratch(const dec_handle* h, size_t* part_floats, size_t* counters) {
+    *part_floats = attn_part_floats(h->rows, h->cfg.n_heads, h->cfg.head_dim, h->attn.empty() ? 0 : h->attn[0].p.nsplit);
+    *counters = (size_t)h->rows * h->cfg.n_kv_heads;
+}
+
+int engine_gate(dec_handle* h) { return gate(h, true); }
+int engine_fail(dec_handle* h, int code, const char* msg) { return fail(h, code, "%s", msg); }
+int engine_device(const dec_handle* h) { return h->cfg.device; }
+
 }  // namespace gd
 
 extern "C" {

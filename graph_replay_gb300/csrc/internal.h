@@ -137,6 +137,9 @@ namespace gd {
 // engine services for other translation units of the library
 int engine_run_attention(dec_handle* h, int32_t layer, const float* qkv, const int32_t* pos, float* out, float* part,
                          unsigned* counters);
-
+void engine_attention_scratch(const dec_handle* h, size_t* part_floats, size_t* counters);
+int engine_gate(dec_handle* h);
+int engine_fail(dec_handle* h, int code, const char* msg);
+int engine_device(const dec_handle* h);
 
 }  // namespace gd

@@ -243,6 +243,22 @@ int dec_kv_ptr(dec_handle *h, int32_t layer, int32_t which, void **ptr, size_t *
  * device check fails (the handle then needs dec_reset_state). */
 int dec_attention(dec_handle *h, int32_t layer, const float *qkv, const int32_t *pos, float *out);
 
+/* dec_attention without any allocation.  Same operation, arguments and
+ * results as dec_attention; the split scratch (partials and completion
+ * counters) lives in a fixed device array inside the library instead of the
+ * handle's workspace, so this call allocates nothing -- for callers that
+ * cannot allocate where they run attention (inside a stream capture, from a
+ * fixed device-memory budget, or where an allocation's implicit device
+ * synchronisation is not acceptable).  The pages have no counterpart of this
+ * entry point.
+ * Limits: the array holds 2^19 fp32 partials and 1024 counters; a shape that
+ * needs more returns DEC_E_UNSUPPORTED.  Every GPU that loads the library keeps
+ * the array until the library is unloaded.  All calls on a device share the
+ * array (it keeps the last call's contents; the counters are cleared on entry),
+ * so calls that overlap on the GPU race.  The first call on a device looks up
+ * the array's device address: make it before any stream capture. */
+int dec_attention_static(dec_handle *h, int32_t layer, const float *qkv, const int32_t *pos, float *out);
+
 /* Device address of the logits [rows, vocab] fp32 of the last step. */
 int dec_logits_ptr(dec_handle *h, float **ptr);
 
