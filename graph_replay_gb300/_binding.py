@@ -30,6 +30,8 @@ DEC_DTYPE_F32 = 0
 DEC_DTYPE_BF16 = 1
 DEC_KV_CONTIGUOUS = 0
 DEC_KV_PAGED = 1
+DEC_STRATEGY_GRAPH = 0
+DEC_STRATEGY_PERSISTENT = 1
 
 (DEC_W_EMBED, DEC_W_ATTN_NORM, DEC_W_Q, DEC_W_K, DEC_W_V, DEC_W_O, DEC_W_FFN_NORM, DEC_W_GATE, DEC_W_UP,
  DEC_W_DOWN, DEC_W_FINAL_NORM, DEC_W_LM_HEAD) = range(12)
@@ -55,7 +57,7 @@ class dec_stats(ctypes.Structure):
                 ("attn_splits", ctypes.c_int32), ("attn_split_len", ctypes.c_int32),
                 ("last_fault", ctypes.c_uint32), ("state", ctypes.c_int32), ("captured", ctypes.c_int32),
                 ("rows", ctypes.c_int32), ("cap", ctypes.c_int32), ("kv_layout", ctypes.c_int32),
-                ("last_step_us", ctypes.c_double), ("workspace_bytes", ctypes.c_int64),
+                ("strategy", ctypes.c_int32), ("reserved", ctypes.c_int32), ("last_step_us", ctypes.c_double), ("workspace_bytes", ctypes.c_int64),
                 ("kv_bytes", ctypes.c_int64)]
 
 
@@ -73,6 +75,7 @@ _SIG = [
     ("dec_step", ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P]),
     ("dec_launch", ctypes.c_int, [_P, _P]),
     ("dec_wait", ctypes.c_int, [_P, _P, _P, _P]),
+    ("dec_set_strategy", ctypes.c_int, [_P, _I32]),
     ("dec_set_eager", ctypes.c_int, [_P, _I32]),
     ("dec_reset_state", ctypes.c_int, [_P]),
     ("dec_kv_ptr", ctypes.c_int, [_P, _I32, _I32, ctypes.POINTER(_P), ctypes.POINTER(ctypes.c_size_t)]),
@@ -182,6 +185,10 @@ def dec_launch(h, dev_slots_ptr) -> int:
 
 def dec_wait(h, logits_ptr, ids_ptr, nonfinite_ptr) -> int:
     return lib().dec_wait(h, logits_ptr, ids_ptr, nonfinite_ptr)
+
+
+def dec_set_strategy(h, strategy: int) -> None:
+    check(h, lib().dec_set_strategy(h, strategy))
 
 
 def dec_set_eager(h, eager: bool) -> None:

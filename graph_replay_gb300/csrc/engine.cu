@@ -49,7 +49,8 @@ int es_of(int dtype) { return dtype == DEC_DTYPE_BF16 ? 2 : 4; }
 
 // Offsets of every buffer of a capture inside one workspace.
 struct WsLayout {
-    size_t status, slots, slot_map, counters, trace, x, qkv, attn, gu, logits, part, rope, kv, kv_layer, total;
+    size_t status, slots, slot_map, counters, trace, ptabs, tmaps, gbar, x, qkv, attn, gu, logits, part, rope, kv,
+        kv_layer, total;
 };
 
 // kernels recorded per step: embedding, 5 per layer, head
@@ -66,6 +67,10 @@ bool compute_layout(const dec_config& c, int cap, int R, int layout, int page, i
     L->slot_map = take(layout == DEC_KV_PAGED ? (size_t)R * (cap / page) * sizeof(int32_t) : 0);
     L->counters = take((size_t)R * Hkv * sizeof(unsigned));
     L->trace = take((1 + 4 * (size_t)kernels_per_step(c.n_layers)) * sizeof(unsigned long long));
+    // persistent-kernel tables: weight and KV pointers, tensor maps, grid counters
+    L->ptabs = take((size_t)c.n_layers * 11 * sizeof(void*));
+    L->tmaps = take(persist_tmap_bytes(c.n_layers));
+    L->gbar = take(((size_t)kernels_per_step(c.n_layers) + 2) * sizeof(unsigned));
     L->x = take((size_t)R * d * 4);
     L->qkv = take((size_t)R * (Hq + 2 * Hkv) * hd * 4);
     L->attn = take((size_t)R * Hq * hd * 4);
@@ -94,6 +99,8 @@ struct dec_handle {
     int num_sms = 0;
     bool pdl = true;
     bool eager = false;
+    int strategy = DEC_STRATEGY_GRAPH;
+    PersistPlan persist;
 
     // weights by role
     const void* embed = nullptr;
@@ -264,6 +271,7 @@ cudaError_t launch_attn(const AttnPlan& a, cudaStream_t s, bool pdl) {
 
 // launch the whole step (the sequence the graph records)
 cudaError_t enqueue_step(dec_handle* h) {
+    if (h->strategy == DEC_STRATEGY_PERSISTENT) return persist_launch(h->persist, h->stream);
     cudaError_t e = embed_launch(h->cfg.weight_dtype == DEC_DTYPE_BF16 ? W_BF16 : W_F32, h->embed_p, h->stream);
     if (e != cudaSuccess) return e;
     for (int l = 0; l < h->cfg.n_layers; ++l) {
@@ -283,6 +291,9 @@ cudaError_t zero_state(dec_handle* h) {
         if ((e = cudaMemsetAsync(h->V[l], 0, h->lay.kv_layer, h->stream)) != cudaSuccess) return e;
     }
     if ((e = cudaMemsetAsync(h->d_status, 0, sizeof(StatusBlock), h->stream)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(h->ws + h->lay.gbar, 0, ((size_t)h->kernels + 2) * sizeof(unsigned), h->stream)) !=
+        cudaSuccess)
+        return e;
     if ((e = cudaMemsetAsync(h->d_slots, 0, 3 * sizeof(int32_t) * h->rows, h->stream)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(h->d_counters, 0, sizeof(unsigned) * h->rows * h->cfg.n_kv_heads, h->stream)) != cudaSuccess)
         return e;
@@ -606,6 +617,47 @@ int dec_capture(dec_handle* h, int32_t cap, int32_t rows, int32_t kv_layout, int
     h->kernels = kernels_per_step(c.n_layers);
     if ((e = cudaMemsetAsync(h->d_trace, 0, sizeof(unsigned long long), h->stream)) != cudaSuccess)
         return cuda_fail(h, e, "trace clear");
+    if (h->strategy == DEC_STRATEGY_PERSISTENT) {
+        if (c.weight_dtype != DEC_DTYPE_BF16 || c.kv_dtype != DEC_DTYPE_BF16)
+            return fail(h, DEC_E_UNSUPPORTED, "the persistent strategy needs bf16 weights and KV");
+        PersistParams& pp = h->persist.p;
+        pp = PersistParams{};
+        pp.L = c.n_layers; pp.d = d; pp.F = F; pp.V = c.vocab; pp.Hq = Hq; pp.Hkv = Hkv; pp.hd = hd;
+        pp.R = rows; pp.cap = cap;
+        pp.paged = kv_layout == DEC_KV_PAGED; pp.page = h->page > 0 ? h->page : 1;
+        pp.pages_per_row = h->ppr; pp.num_pages = h->npages;
+        pp.eps = (float)c.rms_eps; pp.scale = (float)(1.0 / std::sqrt((double)hd));
+        void** ptab = (void**)(h->ws + L.ptabs);
+        pp.lw = (const void* const*)ptab;
+        pp.kv = (void* const*)(ptab + 9 * (size_t)c.n_layers);
+        pp.embed = h->embed; pp.final_norm = h->final_norm; pp.lm_head = h->lm_head;
+        pp.x = h->d_x; pp.qkv = h->d_qkv; pp.attn = h->d_attn; pp.gu = h->d_gu; pp.logits = h->d_logits;
+        pp.part = h->d_part; pp.counters = h->d_counters; pp.slots = h->d_slots; pp.slot_map = h->d_slot_map;
+        pp.rope = h->d_rope; pp.tmaps = h->ws + L.tmaps;
+        pp.err = &h->d_status->err; pp.amax = h->d_status->amax; pp.nonfinite = h->d_status->nonfinite;
+        pp.bar = (unsigned*)(h->ws + L.gbar); pp.trace = h->d_trace;
+        if ((e = persist_plan(&h->persist, h->num_sms)) != cudaSuccess)
+            return fail(h, DEC_E_UNSUPPORTED, "no persistent step kernel for this shape (%s)", cudaGetErrorString(e));
+        std::vector<const void*> host_tab((size_t)c.n_layers * 11);
+        for (int l = 0; l < c.n_layers; ++l) {
+            for (int k = 0; k < 9; ++k) host_tab[(size_t)l * 9 + k] = h->lw[l][k];
+            host_tab[9 * (size_t)c.n_layers + 2 * l] = h->K[l];
+            host_tab[9 * (size_t)c.n_layers + 2 * l + 1] = h->V[l];
+        }
+        if ((e = cudaMemcpy(ptab, host_tab.data(), host_tab.size() * sizeof(void*), cudaMemcpyHostToDevice)) !=
+            cudaSuccess)
+            return cuda_fail(h, e, "persistent table upload");
+        std::vector<unsigned char> tm(persist_tmap_bytes(c.n_layers));
+        std::vector<void*> kvp(2 * (size_t)c.n_layers);
+        for (int l = 0; l < c.n_layers; ++l) {
+            kvp[2 * l] = h->K[l];
+            kvp[2 * l + 1] = h->V[l];
+        }
+        if ((e = persist_tmaps(pp, kvp.data(), tm.data())) != cudaSuccess)
+            return fail(h, DEC_E_UNSUPPORTED, "tensor maps for the persistent kernel (%s)", cudaGetErrorString(e));
+        if ((e = cudaMemcpy(h->ws + L.tmaps, tm.data(), tm.size(), cudaMemcpyHostToDevice)) != cudaSuccess)
+            return cuda_fail(h, e, "tensor map upload");
+    }
 
     // ---- one eager step (launch checks), then a clean state ----
     if ((e = zero_state(h)) != cudaSuccess) return cuda_fail(h, e, "state clear");
@@ -710,6 +762,16 @@ int dec_wait(dec_handle* h, float* logits_out, int32_t* ids_out, uint8_t* nonfin
     return finish_step(h, logits_out, ids_out, nonfinite_out);
 }
 
+int dec_set_strategy(dec_handle* h, int32_t strategy) {
+    int rc = gate(h, false);
+    if (rc) return rc;
+    if (h->captured) return fail(h, DEC_E_STATE, "the strategy is chosen before dec_capture");
+    if (strategy != DEC_STRATEGY_GRAPH && strategy != DEC_STRATEGY_PERSISTENT)
+        return fail(h, DEC_E_INVALID, "unknown strategy %d", strategy);
+    h->strategy = strategy;
+    return DEC_OK;
+}
+
 int dec_set_eager(dec_handle* h, int32_t eager) {
     int rc = gate(h, false);
     if (rc) return rc;
@@ -765,10 +827,13 @@ int dec_stats_get(const dec_handle* h, dec_stats* out) {
     out->steps = h->steps;
     out->replays = h->replays;
     out->eager_steps = h->eager_steps;
-    out->kernels_per_step = h->kernels;
+    out->kernels_per_step = h->strategy == DEC_STRATEGY_PERSISTENT ? 1 : h->kernels;
     out->graph_nodes = (int32_t)h->nodes;
-    out->attn_splits = h->attn.empty() ? 0 : h->attn[0].p.nsplit;
-    out->attn_split_len = h->attn.empty() ? 0 : h->attn[0].p.split_len;
+    out->attn_splits = h->strategy == DEC_STRATEGY_PERSISTENT ? h->persist.p.nsplit
+                                                              : (h->attn.empty() ? 0 : h->attn[0].p.nsplit);
+    out->attn_split_len = h->strategy == DEC_STRATEGY_PERSISTENT ? h->persist.p.split_len
+                                                                 : (h->attn.empty() ? 0 : h->attn[0].p.split_len);
+    out->strategy = h->strategy;
     out->last_fault = h->last_fault;
     out->state = h->state;
     out->captured = h->captured ? 1 : 0;
@@ -785,6 +850,21 @@ int dec_launch_kernel(dec_handle* h, int32_t index, int32_t pdl, int64_t* bytes)
     int rc = gate(h, true);
     if (rc) return rc;
     const int L = h->cfg.n_layers;
+    if (h->strategy == DEC_STRATEGY_PERSISTENT) {
+        if (index != 0) return fail(h, DEC_E_INVALID, "the persistent strategy records one kernel (index 0)");
+        cudaError_t e = persist_launch(h->persist, h->stream);
+        if (e != cudaSuccess) return cuda_fail(h, e, "kernel launch");
+        if (bytes) {
+            const dec_config& c = h->cfg;
+            *bytes = (int64_t)(h->lay.kv_layer * 0);
+            const int64_t wes = 2, R = h->rows;
+            const int64_t d = c.d_model, F = c.ffn_hidden, V = c.vocab, qd = (int64_t)c.n_heads * c.head_dim,
+                          kvd = (int64_t)c.n_kv_heads * c.head_dim;
+            const int64_t per_layer = (qd + 2 * kvd) * d + d * qd + 3 * F * d + 2 * d;
+            *bytes = wes * (L * per_layer + V * d + d + R * d) + R * L * 2 * (int64_t)h->cap * kvd * 2;
+        }
+        return DEC_OK;
+    }
     if (index < 0 || index > 5 * L + 1) return fail(h, DEC_E_INVALID, "kernel index %d outside [0, %d]", index, 5 * L + 1);
     const dec_config& c = h->cfg;
     const int64_t wes = es_of(c.weight_dtype), kes = es_of(c.kv_dtype), R = h->rows;

@@ -130,6 +130,51 @@ cudaError_t embed_launch(int wtype, const EmbedParams& p, cudaStream_t s);
 // a kernel that spins for about `ns` nanoseconds on one SM, then returns
 cudaError_t busy_launch(long long ns, cudaStream_t s);
 
+// ---------------- the whole step as one persistent kernel ----------------
+struct PersistParams {
+    int L, d, F, V, Hq, Hkv, hd, R, cap;
+    int paged, page, pages_per_row, num_pages;
+    float eps, scale;
+    const void* const* lw;     // [L * 9] device table: attn_norm, q, k, v, o, ffn_norm, gate, up, down
+    const void* embed;
+    const void* final_norm;
+    const void* lm_head;
+    float* x;
+    float* qkv;
+    float* attn;
+    float* gu;
+    float* logits;
+    float* part;
+    unsigned* counters;        // [R * Hkv] split completion
+    const int* slots;          // tokens [R], pos [R], write map [R]
+    const int* slot_map;
+    const float2* rope;
+    void* const* kv;           // [L * 2] device table: K, V store of each layer
+    const void* tmaps;         // [L][K|V][2] tensor maps in device memory (64-byte aligned)
+    unsigned* err;
+    unsigned long long* amax;
+    unsigned* nonfinite;
+    unsigned* bar;             // [5L + 4]: per-phase arrivals, exit counter, abort word
+    unsigned long long* trace;
+    int split_len, nsplit;
+    int rps_d, rps_f;          // weight rows per ring stage for K = d and K = F
+};
+
+struct PersistPlan {
+    PersistParams p;
+    int grid = 0, block = 0;
+    size_t smem = 0;
+    const void* fn = nullptr;
+};
+
+// fills split_len / nsplit / rps_* and the launch shape; cudaErrorNotSupported
+// when this shape has no persistent kernel
+cudaError_t persist_plan(PersistPlan* plan, int num_sms);
+size_t persist_tmap_bytes(int n_layers);
+// host images of the layer tensor maps (written to the device table by the caller)
+cudaError_t persist_tmaps(const PersistParams& p, void* const* kv, void* host_out);
+cudaError_t persist_launch(const PersistPlan& plan, cudaStream_t s);
+
 }  // namespace gd
 
 struct dec_handle;

@@ -1,0 +1,937 @@
+// persist.cu -- the whole decode step as one persistent kernel (sm_103a).
+//
+// The pages' own strategy records the step's dispatch sequence and replays it
+// ("Execution", "A constant-shape decode graph"; "Backends", "PTX (NVIDIA)");
+// they name a megakernel as a possible future strategy ("Architecture
+// Overview", "Current state").  This file is that alternative, built for
+// comparison: one cooperative kernel (one CTA per SM) runs every phase of the
+// step -- embedding; per layer RMSNorm+QKV, attention, O-proj, RMSNorm+gate/up,
+// SwiGLU+down; final norm + head + argmax -- and is captured as the graph's
+// single node, replayed per token exactly like the multi-kernel graph.
+//
+// Why it is faster on this GPU: a phase moves 32-235 MB, so each kernel
+// boundary of the multi-kernel graph costs a ramp-up and a tail of several
+// microseconds with HBM partly idle.  Here thread 0 of each CTA streams the
+// CTA's whole step -- every phase's weight rows and K/V tiles, in phase order
+// -- through one ring of shared-memory stages (64 KB, bulk and TMA-tensor
+// copies).  The data of the next phase is already landing while the CTA waits
+// for the phase's grid-wide dependency, so the memory stream never stops.
+//
+// Phase dependencies are grid-wide counters: a CTA adds 1 to its phase's
+// counter after writing the phase's outputs (release fence), and waits until
+// a phase's counter reaches the grid size before reading that phase's outputs
+// (acquire load, bounded poll).  Data written by other CTAs is read through
+// L2 (ld.global.cg).  The cooperative launch guarantees that every CTA is
+// resident, so the waits always end; every wait is still bounded and sets
+// FAULT_WAIT (plus a grid-wide abort word) if it gives up.  The last CTA to
+// finish resets the counters for the next replay.
+//
+// The arithmetic of each phase is the multi-kernel graph's (gemv_impl.cuh and
+// attn_mma.cu): fixed-order reductions, no floating-point atomics, so the
+// results do not depend on scheduling.
+#include <cuda.h>
+#include <math.h>
+#include "common.cuh"
+#include "internal.h"
+#include "mma_helpers.cuh"
+
+namespace gd {
+
+constexpr int PS_WARPS = 16;
+constexpr int PS_THREADS = PS_WARPS * 32;
+constexpr int PS_SL = 8;                   // K-slices
+constexpr int PS_GR = 2;                   // row groups (alternate rows of a stage)
+constexpr int PS_SLOT = 65536;             // bytes per ring slot
+constexpr int PS_S = 3;                    // ring slots
+constexpr int PS_MAX_RPS = 32;
+constexpr int PS_MAX_RES = 64;
+constexpr int PS_AW = 4;                   // warps that compute attention
+constexpr int PS_MAX_L = 64;               // layers whose weight pointers fit the smem table
+constexpr int PS_MAX_NS = 64;              // attention splits per (row, kv head)
+constexpr uint32_t PS_SPIN = 1u << 24;     // polls of a grid-wide wait
+
+enum { PK_EMBED = 0, PK_QKV = 1, PK_ATTN = 2, PK_O = 3, PK_GU = 4, PK_DOWN = 5, PK_HEAD = 6 };
+
+__device__ __forceinline__ float4 ldcg4(const float* p) { return __ldcg(reinterpret_cast<const float4*>(p)); }
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+struct PsShared {
+    uint64_t full_bar[PS_S];
+    int abort;
+    int last;
+    const void* wtab[PS_MAX_L * 9];
+    float red[2][PS_MAX_RPS][PS_SL];
+    float nrm[PS_WARPS];
+    float res[PS_MAX_RES];
+    float wm[PS_AW][8], wl[PS_AW][8];
+    float cm[8 * PS_MAX_NS], cw[8 * PS_MAX_NS];
+};
+
+// geometry of a GEMV phase: up to three stacked weight segments
+struct GvGeom {
+    const void* w[3];
+    int n[3];
+    int N, K, rps;
+};
+
+template <int HD, int G, bool PAGED>
+struct PsState {
+    const PersistParams& P;
+    PsShared& sh;
+    unsigned char* ring;
+    int cta, nc, np, tid;
+    int cons;   // stages consumed (uniform over the CTA)
+    // issue cursor, thread 0 only
+    int iss_p, iss_loc, iss_tot, iss_nst;
+
+    static constexpr int PPS = PS_SLOT / (2 * HD * 2);   // keys per full attention stage
+    static constexpr int TILE = PPS * HD * 2;            // bytes of the K (or V) tile
+    static constexpr int SUB = HD / 64;
+
+    __device__ PsState(const PersistParams& p, PsShared& s, unsigned char* r)
+        : P(p), sh(s), ring(r), cta(blockIdx.x), nc(gridDim.x), np(5 * p.L + 2), tid(threadIdx.x), cons(0),
+          iss_p(0), iss_loc(0), iss_tot(0), iss_nst(-1) {}
+
+    __device__ int kind(int p) const { return p == 0 ? PK_EMBED : (p == np - 1 ? PK_HEAD : 1 + (p - 1) % 5); }
+    __device__ int layer(int p) const { return (p - 1) / 5; }
+    __device__ void rows_of(int N, int& r0, int& r1) const {
+        r0 = (int)(((long long)cta * N) / nc);
+        r1 = (int)(((long long)(cta + 1) * N) / nc);
+    }
+    __device__ void geom(int k, int l, GvGeom& g) const {
+        const void* const* w = sh.wtab + l * 9;   // attn_norm, q, k, v, o, ffn_norm, gate, up, down
+        const int qd = P.Hq * HD, kvd = P.Hkv * HD;
+        g.w[1] = g.w[2] = nullptr;
+        g.n[1] = g.n[2] = 0;
+        switch (k) {
+            case PK_QKV: g.w[0] = w[1]; g.n[0] = qd; g.w[1] = w[2]; g.n[1] = kvd; g.w[2] = w[3]; g.n[2] = kvd;
+                         g.K = P.d; g.rps = P.rps_d; break;
+            case PK_O:   g.w[0] = w[4]; g.n[0] = P.d; g.K = qd; g.rps = P.rps_d; break;
+            case PK_GU:  g.w[0] = w[6]; g.n[0] = P.F; g.w[1] = w[7]; g.n[1] = P.F; g.K = P.d; g.rps = P.rps_d; break;
+            case PK_DOWN: g.w[0] = w[8]; g.n[0] = P.d; g.K = P.F; g.rps = P.rps_f; break;
+            default:     g.w[0] = P.lm_head; g.n[0] = P.V; g.K = P.d; g.rps = P.rps_d; break;
+        }
+        g.N = g.n[0] + g.n[1] + g.n[2];
+    }
+    __device__ int units() const { return P.R * P.Hkv * P.nsplit; }
+    __device__ int unit_len(int u) const {
+        const int s = u % P.nsplit;
+        const int j0 = s * P.split_len;
+        return min(j0 + P.split_len, P.cap) - j0;
+    }
+    __device__ int unit_stages(int u) const { return (unit_len(u) + PPS - 1) / PPS; }
+    __device__ int stages(int p) const {
+        const int k = kind(p);
+        if (k == PK_EMBED) return 0;
+        if (k == PK_ATTN) {
+            int n = 0;
+            for (int u = cta; u < units(); u += nc) n += unit_stages(u);
+            return n;
+        }
+        GvGeom g;
+        geom(k, k == PK_HEAD ? 0 : layer(p), g);
+        int r0, r1;
+        rows_of(g.N, r0, r1);
+        return (r1 - r0 + g.rps - 1) / g.rps;
+    }
+
+    __device__ const CUtensorMap* tmap(int l, int which, int box) const {
+        return reinterpret_cast<const CUtensorMap*>(P.tmaps) + (l * 2 + which) * 2 + box;
+    }
+
+    // thread 0: issue the next stage of the CTA's whole-step stream
+    __device__ void issue_next() {
+        while (iss_p < np) {
+            if (iss_nst < 0) iss_nst = stages(iss_p);
+            if (iss_loc < iss_nst) break;
+            ++iss_p;
+            iss_loc = 0;
+            iss_nst = -1;
+        }
+        if (iss_p >= np) return;
+        const int slot = iss_tot % PS_S;
+        uint64_t* bar = &sh.full_bar[slot];
+        unsigned char* dst = ring + (size_t)slot * PS_SLOT;
+        const int k = kind(iss_p);
+        if (k == PK_ATTN) {
+            const int l = layer(iss_p);
+            int loc = iss_loc, u = cta;
+            while (loc >= unit_stages(u)) {
+                loc -= unit_stages(u);
+                u += nc;
+            }
+            const int s = u % P.nsplit, g = (u / P.nsplit) % P.Hkv, r = u / (P.nsplit * P.Hkv);
+            const int j0 = s * P.split_len;
+            const int j1 = min(j0 + P.split_len, P.cap);
+            const int p0 = j0 + loc * PPS, p1 = min(p0 + PPS, j1);
+            const int n = p1 - p0;
+            unsigned char* kd = dst;
+            unsigned char* vd = dst + TILE;
+            mbar_arrive_expect_tx(bar, (uint32_t)(2 * n * HD * 2));
+            if (PAGED) {
+                const int pg_size = P.page;
+                for (int q = p0; q < p1; q += pg_size) {
+                    int pg = P.slot_map[(size_t)r * P.pages_per_row + q / pg_size];
+                    if (pg < 0 || pg >= P.num_pages) pg = 0;   // flagged by the consumers
+                    const int y = (pg * P.Hkv + g) * pg_size;
+#pragma unroll
+                    for (int sb = 0; sb < SUB; ++sb) {
+                        tma_load_2d(kd + sb * PPS * 128 + (q - p0) * 128, tmap(l, 0, 0), sb * 64, y, bar);
+                        tma_load_2d(vd + sb * PPS * 128 + (q - p0) * 128, tmap(l, 1, 0), sb * 64, y, bar);
+                    }
+                }
+            } else {
+                const int y = (r * P.Hkv + g) * P.cap + p0;
+                const int box = n == PPS ? 0 : 1;   // full stage, or the half stage that ends a split
+#pragma unroll
+                for (int sb = 0; sb < SUB; ++sb) {
+                    tma_load_2d(kd + sb * PPS * 128, tmap(l, 0, box), sb * 64, y, bar);
+                    tma_load_2d(vd + sb * PPS * 128, tmap(l, 1, box), sb * 64, y, bar);
+                }
+            }
+        } else {
+            GvGeom gg;
+            geom(k, k == PK_HEAD ? 0 : layer(iss_p), gg);
+            int r0, r1;
+            rows_of(gg.N, r0, r1);
+            const int a = r0 + iss_loc * gg.rps, b = min(a + gg.rps, r1);
+            const size_t rb = (size_t)gg.K * 2;
+            mbar_arrive_expect_tx(bar, (uint32_t)((size_t)(b - a) * rb));
+            int row = a;
+            while (row < b) {
+                int base = 0, sg = 0;
+                while (sg < 2 && row >= base + gg.n[sg]) {
+                    base += gg.n[sg];
+                    ++sg;
+                }
+                const int e = min(b, base + gg.n[sg]);
+                const uint32_t bytes = (uint32_t)((size_t)(e - row) * rb);
+                bulk_g2s(dst, reinterpret_cast<const unsigned char*>(gg.w[sg]) + (size_t)(row - base) * rb, bytes, bar);
+                dst += bytes;
+                row = e;
+            }
+        }
+        ++iss_loc;
+        ++iss_tot;
+    }
+
+    // consumer side of one stage: wait for it; false after an abort
+    __device__ const unsigned char* stage_wait() {
+        const int slot = cons % PS_S;
+        volatile int* ab = &sh.abort;
+        if (!*ab && !mbar_wait(&sh.full_bar[slot], (cons / PS_S) & 1)) {
+            *ab = 1;
+            atomicOr(P.err, FAULT_WAIT);
+        }
+        return ring + (size_t)slot * PS_SLOT;
+    }
+    // every thread is done with the stage: thread 0 refills the slot
+    __device__ void stage_release() {
+        __syncthreads();
+        if (tid == 0 && !*reinterpret_cast<volatile int*>(&sh.abort)) {
+            fence_proxy_async_smem();   // generic writes to the slot before the async refill
+            issue_next();
+        }
+        ++cons;
+    }
+
+    __device__ void grid_arrive(int p) {
+        __syncthreads();
+        if (tid == 0) {
+            __threadfence();
+            atomicAdd(P.bar + p, 1u);
+        }
+    }
+    __device__ void grid_wait(int p) {
+        if (tid == 0) {
+            volatile unsigned* gab = P.bar + np + 1;
+            bool ok = false;
+            for (uint32_t i = 0; i < PS_SPIN; ++i) {
+                if (ld_acquire(P.bar + p) >= (unsigned)nc) {
+                    ok = true;
+                    break;
+                }
+                if (*gab) break;
+                __nanosleep(40);
+            }
+            if (!ok) {
+                sh.abort = 1;
+                atomicOr(P.err, FAULT_WAIT);
+                atomicExch(const_cast<unsigned*>(gab), 1u);
+            }
+            __threadfence();
+        }
+        __syncthreads();
+    }
+};
+
+// ---------------- GEMV phase ----------------
+template <int CPL, int PRO, int EPI, int HD, int G, bool PAGED>
+__device__ __forceinline__ void ps_gemv(PsState<HD, G, PAGED>& st, const GvGeom& g, const float* act,
+                                        int act_stride, const __nv_bfloat16* gain, float* out, int out_stride) {
+    constexpr int VEC = 8;
+    constexpr int RU = 8 / CPL;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int K = g.K;
+    const int SWV = K / (PS_SL * VEC);
+    const int slice = warp % PS_SL, grp = warp / PS_SL;
+    const int vbase = slice * SWV;
+    int row0, row1;
+    st.rows_of(g.N, row0, row1);
+    const int rps = g.rps;
+    const int nst = (row1 - row0 + rps - 1) / rps;
+    const size_t row_bytes = (size_t)K * 2;
+    PsShared& sh = st.sh;
+
+    // prologue: activations of this lane's columns, in registers
+    float inv = 1.f;
+    if (PRO == PRO_RMSNORM) {
+        float ss = 0.f;
+        for (int k = tid * 4; k < K; k += PS_THREADS * 4) {
+            const float4 x = ldcg4(act + k);
+            ss = fmaf(x.x, x.x, ss);
+            ss = fmaf(x.y, x.y, ss);
+            ss = fmaf(x.z, x.z, ss);
+            ss = fmaf(x.w, x.w, ss);
+        }
+        ss = warp_sum(ss);
+        if (lane == 0) sh.nrm[warp] = ss;
+        __syncthreads();
+        float t = 0.f;
+#pragma unroll
+        for (int w = 0; w < PS_WARPS; ++w) t += sh.nrm[w];
+        inv = 1.0f / sqrtf(t / (float)K + st.P.eps);
+    }
+    float areg[CPL][VEC];
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) {
+        const int c = (vbase + lane + 32 * j) * VEC;
+        const float4 x0 = ldcg4(act + c), x1 = ldcg4(act + c + 4);
+        float o[VEC] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        if (PRO == PRO_RMSNORM) {
+            float gf[VEC];
+            Elem<__nv_bfloat16>::unpack(*reinterpret_cast<const uint4*>(gain + c), gf);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) o[e] = o[e] * inv * gf[e];
+        } else if (PRO == PRO_SWIGLU) {
+            const float4 u0 = ldcg4(act + K + c), u1 = ldcg4(act + K + c + 4);
+            const float uu[VEC] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) o[e] = o[e] / (1.0f + expf(-o[e])) * uu[e];
+        }
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) areg[j][e] = o[e];
+    }
+    const bool res_local = EPI == EPI_ADD && (row1 - row0) <= PS_MAX_RES;
+    if (EPI == EPI_ADD && res_local)
+        for (int i = tid; i < row1 - row0; i += PS_THREADS) sh.res[i] = __ldcg(out + row0 + i);
+    if (EPI == EPI_ADD) __syncthreads();
+
+    unsigned long long best = 0ull;
+    bool nonfin = false;
+    for (int k = 0; k < nst; ++k) {
+        const int a = row0 + k * rps;
+        const int nr = min(rps, row1 - a);
+        const unsigned char* stg = st.stage_wait();
+        const bool live = !*reinterpret_cast<volatile int*>(&sh.abort);
+        const int nmine = nr > grp ? (nr - grp + PS_GR - 1) / PS_GR : 0;
+        for (int m0 = 0; m0 < nmine; m0 += RU) {
+            float acc[RU], acc2[RU];
+#pragma unroll
+            for (int u = 0; u < RU; ++u) acc[u] = acc2[u] = 0.f;
+            if (live) {
+                // slices are exactly 32 * CPL vectors wide (the plan admits no other K);
+                // a row group's last rows past nmine re-read its last row, results dropped
+                uint4 wv[RU][CPL];
+#pragma unroll
+                for (int u = 0; u < RU; ++u) {
+                    const int iu = grp + PS_GR * min(m0 + u, nmine - 1);
+                    const uint4* wr = reinterpret_cast<const uint4*>(stg + (size_t)iu * row_bytes);
+#pragma unroll
+                    for (int j = 0; j < CPL; ++j) wv[u][j] = wr[vbase + lane + 32 * j];
+                }
+#pragma unroll
+                for (int u = 0; u < RU; ++u)
+#pragma unroll
+                    for (int j = 0; j < CPL; ++j) {
+                        float wf[VEC];
+                        Elem<__nv_bfloat16>::unpack(wv[u][j], wf);
+#pragma unroll
+                        for (int e = 0; e < VEC; e += 2) {
+                            acc[u] = fmaf(wf[e], areg[j][e], acc[u]);
+                            acc2[u] = fmaf(wf[e + 1], areg[j][e + 1], acc2[u]);
+                        }
+                    }
+            }
+#pragma unroll
+            for (int u = 0; u < RU; ++u) {
+                const float t = warp_sum(acc[u] + acc2[u]);
+                if (lane == 0 && m0 + u < nmine) sh.red[k & 1][grp + PS_GR * (m0 + u)][slice] = t;
+            }
+        }
+        st.stage_release();
+        if (warp == 0 && lane < nr && live) {
+            const int row = a + lane;
+            float t = 0.f;
+#pragma unroll
+            for (int w = 0; w < PS_SL; ++w) t += sh.red[k & 1][lane][w];
+            if (EPI == EPI_ADD) {
+                out[row] = (res_local ? sh.res[row - row0] : __ldcg(out + row)) + t;
+            } else {
+                out[row] = t;
+            }
+            if (EPI == EPI_LOGITS) {
+                if (!isfinite(t)) nonfin = true;
+                const unsigned long long key = argmax_key(t, row);
+                best = key > best ? key : best;
+            }
+        }
+    }
+    if (EPI == EPI_LOGITS && warp == 0) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
+            best = other > best ? other : best;
+        }
+        const bool any_nf = __any_sync(0xffffffffu, nonfin);
+        if (lane == 0) {
+            if (best) atomicMax(st.P.amax, best);
+            if (any_nf) atomicOr(st.P.nonfinite, 1u);
+        }
+    }
+}
+
+// ---------------- attention phase (tensor cores, as attn_mma.cu) ----------------
+template <int HD, int G, bool PAGED>
+__device__ __forceinline__ void ps_attention(PsState<HD, G, PAGED>& st, int l, float* q_s, float* kn_s, float* vn_s,
+                                             float* wo_s, __nv_bfloat16* qt_s) {
+    using ST = PsState<HD, G, PAGED>;
+    constexpr int PPS = ST::PPS, TILE = ST::TILE;
+    constexpr int KPW = PPS / PS_AW, BLK = KPW / 16, KSTEP = HD / 16, DT = HD / 16;
+    static_assert(G <= 4, "P^T columns hold G heads' bf16 parts and G remainders");
+    const PersistParams& P = st.P;
+    PsShared& sh = st.sh;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int gq = lane >> 2, tq = lane & 3;
+    __nv_bfloat16* Kc = reinterpret_cast<__nv_bfloat16*>(P.kv[2 * l]);
+    __nv_bfloat16* Vc = reinterpret_cast<__nv_bfloat16*>(P.kv[2 * l + 1]);
+    const int Pg = P.page;
+
+    for (int u = st.cta; u < st.units(); u += st.nc) {
+        const int s = u % P.nsplit, g = (u / P.nsplit) % P.Hkv, r = u / (P.nsplit * P.Hkv);
+        const int j0 = s * P.split_len;
+        const int j1 = min(j0 + P.split_len, P.cap);
+        const int nst = (j1 - j0 + PPS - 1) / PPS;
+        int pos = P.slots[P.R + r];
+        pos = min(max(pos, 0), P.cap - 1);
+        const float* qrow = P.qkv + (size_t)r * (P.Hq + 2 * P.Hkv) * HD;
+        const float2* rt = P.rope + (size_t)pos * (HD / 2);
+        if (PAGED) {   // page ids this unit's producer read
+            for (int q = j0 + tid * Pg; q < j1; q += PS_THREADS * Pg) {
+                const int pg = P.slot_map[(size_t)r * P.pages_per_row + q / Pg];
+                if (pg < 0 || pg >= P.num_pages) atomicOr(P.err, FAULT_SLOT_MAP);
+            }
+        }
+        for (int i = tid; i < G * (HD / 2); i += PS_THREADS) {
+            const int h = i / (HD / 2), d = i % (HD / 2);
+            const float* qh = qrow + (size_t)(g * G + h) * HD;
+            const float a = __ldcg(qh + d), b = __ldcg(qh + d + HD / 2);
+            const float2 cs = rt[d];
+            q_s[h * HD + d] = (a * cs.x - b * cs.y) * P.scale;
+            q_s[h * HD + d + HD / 2] = (a * cs.y + b * cs.x) * P.scale;
+        }
+        const bool owner = pos >= j0 && pos < j1;
+        if (owner) {
+            const float* kh = qrow + (size_t)P.Hq * HD + (size_t)g * HD;
+            const float* vh = kh + (size_t)P.Hkv * HD;
+            size_t off;
+            bool ok = true;
+            if (PAGED) {
+                const int slot = P.slots[2 * P.R + r];
+                if (slot < 0 || slot >= P.num_pages * Pg) {
+                    ok = false;
+                    if (tid == 0) atomicOr(P.err, FAULT_WRITE_MAP);
+                }
+                const int pg = ok ? slot / Pg : 0, o = ok ? slot % Pg : 0;
+                off = (((size_t)pg * P.Hkv + g) * Pg + o) * HD;
+            } else {
+                off = (((size_t)r * P.Hkv + g) * P.cap + pos) * HD;
+            }
+            for (int d = tid; d < HD / 2; d += PS_THREADS) {
+                const float a = __ldcg(kh + d), b = __ldcg(kh + d + HD / 2);
+                const float2 cs = rt[d];
+                const float k0 = a * cs.x - b * cs.y, k1 = a * cs.y + b * cs.x;
+                kn_s[d] = ok ? Elem<__nv_bfloat16>::round_store(k0, Kc + off + d) : bf16_round_f(k0);
+                kn_s[d + HD / 2] = ok ? Elem<__nv_bfloat16>::round_store(k1, Kc + off + d + HD / 2) : bf16_round_f(k1);
+            }
+            for (int d = tid; d < HD; d += PS_THREADS) {
+                const float vv = __ldcg(vh + d);
+                vn_s[d] = ok ? Elem<__nv_bfloat16>::round_store(vv, Vc + off + d) : bf16_round_f(vv);
+            }
+        }
+        __syncthreads();
+        // Q as the MMA's A operand, a padded bf16 tile [16][HD + 8]: rows g < G hold
+        // bf16(q) of head g, rows 8 + g the remainder q - bf16(q), the rest zero
+        for (int i = tid; i < 16 * HD; i += PS_THREADS) {
+            const int row = i / HD, col = i % HD, h = row & 7;
+            const float v = h < G ? q_s[h * HD + col] : 0.f;
+            const float hi = bf16_round_f(v);
+            qt_s[row * (HD + 8) + col] = __float2bfloat16_rn(row < 8 ? hi : v - hi);
+        }
+        __syncthreads();
+
+        // O^T accumulators: tile dt covers dims 16dt..16dt+15 (rows g, g + 8) x
+        // columns 2tq, 2tq+1 (columns 0..3: heads' bf16 parts, 4..7: remainders)
+        float m_run = -INFINITY, l_run = 0.f;
+        float o[DT][4];
+        if (warp < PS_AW) {
+#pragma unroll
+            for (int n = 0; n < DT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+        }
+        const int h0 = (2 * tq) & 3, h1 = (2 * tq + 1) & 3;   // heads of this lane's two columns
+
+        for (int t = 0; t < nst; ++t) {
+            unsigned char* kt = const_cast<unsigned char*>(st.stage_wait());
+            unsigned char* vt = kt + TILE;
+            const bool live = !*reinterpret_cast<volatile int*>(&sh.abort);
+            const int p0 = j0 + t * PPS;
+            if (owner && pos >= p0 && pos < p0 + PPS) {   // CTA-uniform
+                const int row = pos - p0;
+                for (int i = tid; i < 2 * (HD / 8); i += PS_THREADS) {
+                    const int c = i % (HD / 8);
+                    const float* src = (i < HD / 8 ? kn_s : vn_s) + c * 8;
+                    uint4 v;
+                    v.x = pack_bf16x2(src[0], src[1]);
+                    v.y = pack_bf16x2(src[2], src[3]);
+                    v.z = pack_bf16x2(src[4], src[5]);
+                    v.w = pack_bf16x2(src[6], src[7]);
+                    *reinterpret_cast<uint4*>((i < HD / 8 ? kt : vt) + swz<HD, PPS>(row, c)) = v;
+                }
+                __syncthreads();
+            }
+            if (live && warp < PS_AW) {
+#pragma unroll
+                for (int b = 0; b < BLK; ++b) {
+                    const int kb = warp * KPW + b * 16;
+                    const int key0 = p0 + kb;
+                    if (key0 > pos || key0 >= j1) continue;
+                    float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+                    for (int ks = 0; ks < KSTEP; ++ks) {
+                        const int mi = lane >> 3, rr = lane & 7;
+                        // A fragments: (rows 0-7 | 8-15) x (cols 16ks..+7 | +8..+15)
+                        uint32_t qa[4];
+                        ldsm_x4(smem_u32(qt_s + (rr + ((mi & 1) << 3)) * (HD + 8) + ks * 16 + ((mi >> 1) << 3)), qa[0],
+                                qa[1], qa[2], qa[3]);
+                        const int krow = kb + rr + ((mi >> 1) << 3);
+                        const int chunk = ks * 2 + (mi & 1);
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4(smem_u32(kt + swz<HD, PPS>(krow, chunk)), b0, b1, b2, b3);
+                        mma_bf16(sacc[0], qa, b0, b1);
+                        mma_bf16(sacc[1], qa, b2, b3);
+                    }
+                    float sc[4];
+                    bool vis[4];
+#pragma unroll
+                    for (int n = 0; n < 2; ++n)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int key = key0 + 8 * n + 2 * tq + e;
+                            vis[2 * n + e] = key <= pos && key < j1;
+                            const float v = sacc[n][e] + sacc[n][2 + e];
+                            sc[2 * n + e] = vis[2 * n + e] ? v : -INFINITY;
+                        }
+                    float mx = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                    const float mn = fmaxf(m_run, mx);
+                    const float alpha = (m_run == -INFINITY) ? 0.f : expf(m_run - mn);
+                    float pr[4];
+                    float ps = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        pr[i] = vis[i] ? expf(sc[i] - mn) : 0.f;
+                        ps += pr[i];
+                    }
+                    l_run = l_run * alpha + ps;
+                    m_run = mn;
+                    // rescale: the lane's columns belong to heads h0, h1 (alpha of head h sits in lanes 4h..4h+3)
+                    const float a0 = __shfl_sync(0xffffffffu, alpha, 4 * h0);
+                    const float a1 = __shfl_sync(0xffffffffu, alpha, 4 * h1);
+#pragma unroll
+                    for (int n = 0; n < DT; ++n) {
+                        o[n][0] *= a0; o[n][1] *= a1; o[n][2] *= a0; o[n][3] *= a1;
+                    }
+                    // P^T as the B operand: column gq < 4 is head gq's bf16(p), column 4 + h
+                    // the remainder p - bf16(p) of head h (taken from lane - 16)
+                    uint32_t pb0, pb1;
+                    {
+                        float pv[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float other = __shfl_xor_sync(0xffffffffu, pr[i], 16);
+                            const int h = gq & 3;
+                            const float v = (gq < 4) ? pr[i] : other;
+                            const float vv = h < G ? v : 0.f;
+                            const float hi = bf16_round_f(vv);
+                            pv[i] = gq < 4 ? hi : vv - hi;
+                        }
+                        pb0 = pack_bf16x2(pv[0], pv[1]);   // keys 2tq, 2tq+1 of the block
+                        pb1 = pack_bf16x2(pv[2], pv[3]);   // keys 8+2tq, 9+2tq
+                    }
+                    const bool partial = key0 + 15 > pos || key0 + 15 >= j1;
+                    const uint32_t keep0 = (vis[0] ? 0x0000FFFFu : 0u) | (vis[1] ? 0xFFFF0000u : 0u);
+                    const uint32_t keep1 = (vis[2] ? 0x0000FFFFu : 0u) | (vis[3] ? 0xFFFF0000u : 0u);
+                    // O^T += V^T P^T: V^T fragments by transposed ldmatrix (rows = dims, k = keys)
+#pragma unroll
+                    for (int dt = 0; dt < DT; ++dt) {
+                        // matrices: (keys 0-7, dims 0-7) a0, (keys 0-7, dims 8-15) a1,
+                        //           (keys 8-15, dims 0-7) a2, (keys 8-15, dims 8-15) a3
+                        const int mi = lane >> 3, rr = lane & 7;
+                        const int vrow = kb + rr + ((mi >> 1) << 3);
+                        const int chunk = dt * 2 + (mi & 1);
+                        uint32_t va[4];
+                        ldsm_x4_t(smem_u32(vt + swz<HD, PPS>(vrow, chunk)), va[0], va[1], va[2], va[3]);
+                        if (partial) {   // masked keys' V become zero by select (this lane's keys = its scores' keys)
+                            va[0] &= keep0;
+                            va[1] &= keep0;
+                            va[2] &= keep1;
+                            va[3] &= keep1;
+                        }
+                        mma_bf16(o[dt], va, pb0, pb1);
+                    }
+                }
+            }
+            st.stage_release();
+        }
+
+        // merge the attention warps (fixed order), write this split's partial
+        if (warp < PS_AW) {
+            float lsum = l_run;
+            lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
+            lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
+            // add the remainder columns (lane + 2 within the quad) to the heads' columns
+#pragma unroll
+            for (int n = 0; n < DT; ++n)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[n][e] += __shfl_xor_sync(0xffffffffu, o[n][e], 2);
+            if (tq < 2) {
+#pragma unroll
+                for (int n = 0; n < DT; ++n) {
+                    if (h0 < G) {
+                        wo_s[(warp * G + h0) * HD + n * 16 + gq] = o[n][0];
+                        wo_s[(warp * G + h0) * HD + n * 16 + gq + 8] = o[n][2];
+                    }
+                    if (h1 < G) {
+                        wo_s[(warp * G + h1) * HD + n * 16 + gq] = o[n][1];
+                        wo_s[(warp * G + h1) * HD + n * 16 + gq + 8] = o[n][3];
+                    }
+                }
+            }
+            if (gq < G && tq == 0) {
+                sh.wm[warp][gq] = m_run;
+                sh.wl[warp][gq] = lsum;
+            }
+        }
+        __syncthreads();
+        for (int i = tid; i < G * HD; i += PS_THREADS) {
+            const int h = i / HD, d = i % HD;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < PS_AW; ++w) M = fmaxf(M, sh.wm[w][h]);
+            float Ls = 0.f, Os = 0.f;
+#pragma unroll
+            for (int w = 0; w < PS_AW; ++w) {
+                const float f = (sh.wm[w][h] == -INFINITY) ? 0.f : expf(sh.wm[w][h] - M);
+                Ls = fmaf(f, sh.wl[w][h], Ls);
+                Os = fmaf(f, wo_s[(w * G + h) * HD + d], Os);
+            }
+            float* pp = P.part + (((size_t)r * P.Hq + g * G + h) * P.nsplit + s) * (HD + 4);
+            pp[4 + d] = Os;
+            if (d == 0) {
+                pp[0] = M;
+                pp[1] = Ls;
+            }
+        }
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) {
+            const unsigned prev = atomicAdd(P.counters + r * P.Hkv + g, 1u);
+            sh.last = prev == (unsigned)P.nsplit - 1u;
+        }
+        __syncthreads();
+        if (sh.last) {
+            __threadfence();
+            if (tid == 0) P.counters[r * P.Hkv + g] = 0u;
+            const int NS = P.nsplit;
+            for (int i = tid; i < G * NS; i += PS_THREADS) {
+                const int h = i / NS, ss = i % NS;
+                const float* pp = P.part + (((size_t)r * P.Hq + g * G + h) * NS + ss) * (HD + 4);
+                sh.cm[h * NS + ss] = __ldcg(pp);
+                sh.cw[h * NS + ss] = __ldcg(pp + 1);
+            }
+            __syncthreads();
+            for (int h = warp; h < G; h += PS_WARPS) {
+                float M = -INFINITY;
+                for (int ss = lane; ss < NS; ss += 32) M = fmaxf(M, sh.cm[h * NS + ss]);
+                M = warp_max(M);
+                float Lsum = 0.f;
+                for (int ss = lane; ss < NS; ss += 32) {
+                    const float mm = sh.cm[h * NS + ss];
+                    Lsum += (mm == -INFINITY) ? 0.f : expf(mm - M) * sh.cw[h * NS + ss];
+                }
+                Lsum = warp_sum(Lsum);
+                for (int ss = lane; ss < NS; ss += 32) {
+                    const float mm = sh.cm[h * NS + ss];
+                    sh.cw[h * NS + ss] = (mm == -INFINITY) ? 0.f : expf(mm - M) / Lsum;
+                }
+            }
+            __syncthreads();
+            for (int i = tid; i < G * HD; i += PS_THREADS) {
+                const int h = i / HD, d = i % HD;
+                const float* base = P.part + (((size_t)r * P.Hq + g * G + h) * NS) * (HD + 4) + 4 + d;
+                float acc = 0.f;
+#pragma unroll 4
+                for (int ss = 0; ss < NS; ++ss) acc = fmaf(sh.cw[h * NS + ss], __ldcg(base + (size_t)ss * (HD + 4)), acc);
+                P.attn[(size_t)r * P.Hq * HD + (size_t)(g * G + h) * HD + d] = acc;
+            }
+        }
+        __syncthreads();
+    }
+}
+
+template <int CPL_D, int CPL_F, int HD, int G, bool PAGED>
+__global__ void __launch_bounds__(PS_THREADS, 1) k_persist(const __grid_constant__ PersistParams P) {
+    extern __shared__ __align__(1024) unsigned char ps_raw[];
+    unsigned char* ring =
+        reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(ps_raw) + 1023) & ~(uintptr_t)1023);
+    __shared__ PsShared sh;
+    __shared__ float q_s[G * HD], kn_s[HD], vn_s[HD];
+    __shared__ float wo_s[PS_AW * G * HD];
+    __shared__ __align__(16) __nv_bfloat16 qt_s[16 * (HD + 8)];
+    using ST = PsState<HD, G, PAGED>;
+    const int tid = threadIdx.x;
+
+    for (int i = tid; i < P.L * 9; i += PS_THREADS) sh.wtab[i] = P.lw[i];
+    if (tid == 0) {
+        for (int s = 0; s < PS_S; ++s) mbar_init(&sh.full_bar[s], 1);
+        sh.abort = 0;
+        mbar_fence_init();
+    }
+    __syncthreads();
+    ST st(P, sh, ring);
+    if (tid == 0)
+        for (int i = 0; i < PS_S; ++i) st.issue_next();   // the stream starts before any dependency
+    const int np = st.np;
+
+    for (int p = 0; p < np; ++p) {
+        const int k = st.kind(p);
+        if (tid == 0) trace_stamp(P.trace, p, 0);
+        if (p > 0) st.grid_wait(p - 1);
+        if (tid == 0) trace_stamp(P.trace, p, 1);
+        if (k == PK_EMBED) {
+            if (st.cta == 0) {
+                // the step's first phase: resets, checks, gather (as k_embed)
+                if (tid == 0) *P.err = 0u;
+                if (tid < P.R) {
+                    P.amax[tid] = 0ull;
+                    P.nonfinite[tid] = 0u;
+                }
+                __syncthreads();
+                for (int r = 0; r < P.R; ++r) {
+                    int tok = P.slots[r];
+                    const int pos = P.slots[P.R + r];
+                    if (tok < 0 || tok >= P.V) {
+                        if (tid == 0) atomicOr(P.err, FAULT_TOKEN);
+                        tok = 0;
+                    }
+                    if ((pos < 0 || pos >= P.cap) && tid == 0) atomicOr(P.err, FAULT_POS);
+                    const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(P.embed) + (size_t)tok * P.d;
+                    for (int i = tid * 8; i < P.d; i += PS_THREADS * 8) {
+                        float f[8];
+                        Elem<__nv_bfloat16>::unpack(*reinterpret_cast<const uint4*>(e + i), f);
+                        *reinterpret_cast<float4*>(P.x + i + (size_t)r * P.d) = make_float4(f[0], f[1], f[2], f[3]);
+                        *reinterpret_cast<float4*>(P.x + i + 4 + (size_t)r * P.d) = make_float4(f[4], f[5], f[6], f[7]);
+                    }
+                }
+            }
+        } else if (k == PK_ATTN) {
+            ps_attention<HD, G, PAGED>(st, st.layer(p), q_s, kn_s, vn_s, wo_s, qt_s);
+        } else {
+            GvGeom g;
+            const int l = k == PK_HEAD ? 0 : st.layer(p);
+            st.geom(k, l, g);
+            const __nv_bfloat16* w9 = nullptr;
+            switch (k) {
+                case PK_QKV:
+                    ps_gemv<CPL_D, PRO_RMSNORM, EPI_STORE>(st, g, P.x, P.d,
+                        reinterpret_cast<const __nv_bfloat16*>(sh.wtab[l * 9 + 0]), P.qkv, g.N);
+                    break;
+                case PK_O:
+                    ps_gemv<CPL_D, PRO_PLAIN, EPI_ADD>(st, g, P.attn, g.K, w9, P.x, P.d);
+                    break;
+                case PK_GU:
+                    ps_gemv<CPL_D, PRO_RMSNORM, EPI_STORE>(st, g, P.x, P.d,
+                        reinterpret_cast<const __nv_bfloat16*>(sh.wtab[l * 9 + 5]), P.gu, g.N);
+                    break;
+                case PK_DOWN:
+                    ps_gemv<CPL_F, PRO_SWIGLU, EPI_ADD>(st, g, P.gu, 2 * P.F, w9, P.x, P.d);
+                    break;
+                default:
+                    ps_gemv<CPL_D, PRO_RMSNORM, EPI_LOGITS>(st, g, P.x, P.d,
+                        reinterpret_cast<const __nv_bfloat16*>(P.final_norm), P.logits, P.V);
+                    break;
+            }
+        }
+        st.grid_arrive(p);
+        if (tid == 0) {
+            trace_stamp(P.trace, p, 2);
+            trace_stamp(P.trace, p, 3);
+        }
+    }
+    // no copy may still be landing when the CTA exits
+    if (tid == 0)
+        for (int i = max(0, st.iss_tot - PS_S); i < st.iss_tot; ++i)
+            if (!mbar_wait(&sh.full_bar[i % PS_S], (i / PS_S) & 1)) atomicOr(P.err, FAULT_WAIT);
+    // the last CTA out resets the grid counters for the next replay
+    if (tid == 0) {
+        __threadfence();
+        const unsigned prev = atomicAdd(P.bar + np, 1u);
+        if (prev == (unsigned)gridDim.x - 1u) {
+            for (int p = 0; p <= np + 1; ++p) P.bar[p] = 0u;
+            __threadfence();
+        }
+    }
+}
+
+// ---------------- host side ----------------
+
+template <int CPL_D, int CPL_F, int HD, int G>
+static const void* ps_pick_paged(bool paged) {
+    return paged ? (const void*)&k_persist<CPL_D, CPL_F, HD, G, true>
+                 : (const void*)&k_persist<CPL_D, CPL_F, HD, G, false>;
+}
+// instantiated shapes: (d, F, hd, G) of the 8B-shape and 1B-class decoders
+static const void* ps_pick(int cpl_d, int cpl_f, int hd, int G, bool paged) {
+    if (cpl_d == 2 && cpl_f == 7 && hd == 128 && G == 4) return ps_pick_paged<2, 7, 128, 4>(paged);
+    if (cpl_d == 1 && cpl_f == 4 && hd == 64 && G == 4) return ps_pick_paged<1, 4, 64, 4>(paged);
+    return nullptr;
+}
+
+static int cpl_of(int K) { return (K / (PS_SL * 8) + 31) / 32; }
+
+cudaError_t persist_plan(PersistPlan* plan, int num_sms) {
+    PersistParams& p = plan->p;
+    if (p.R != 1 || p.L > PS_MAX_L) return cudaErrorNotSupported;
+    if (p.Hq * p.hd != p.d) return cudaErrorNotSupported;   // O-proj uses the d-column variant
+    if (p.d % (PS_SL * 8 * 32) || p.F % (PS_SL * 8 * 32)) return cudaErrorNotSupported;
+    const int cd = cpl_of(p.d), cf = cpl_of(p.F);
+    if (p.d / (PS_SL * 8) != 32 * cd || p.F / (PS_SL * 8) != 32 * cf) return cudaErrorNotSupported;
+    const int G = p.Hq / p.Hkv;
+    const void* fn = ps_pick(cd, cf, p.hd, G, p.paged != 0);
+    if (!fn) return cudaErrorNotSupported;
+    // rows per 64 KB stage (whole rows, a multiple of the row groups' loads)
+    auto rps_for = [&](int K, int cpl) {
+        int r = PS_SLOT / (K * 2);
+        if (r > PS_MAX_RPS) r = PS_MAX_RPS;
+        const int ru = 8 / cpl;
+        if (r >= PS_GR * ru) r -= r % (PS_GR * ru);
+        return r;
+    };
+    p.rps_d = rps_for(p.d, cd);
+    p.rps_f = rps_for(p.F, cf);
+    if (p.rps_d < PS_GR || p.rps_f < PS_GR) return cudaErrorNotSupported;
+    // attention splits: whole half-stages; units spread over the grid
+    const int pps = PS_SLOT / (2 * p.hd * 2), half = pps / 2;
+    if (p.paged ? (pps % p.page != 0 || p.cap % p.page != 0) : (p.cap % half != 0)) return cudaErrorNotSupported;
+    const int units0 = p.R * p.Hkv;
+    long long best = -1;
+    int bl = 0, bn = 0;
+    for (int want = 1; want <= PS_MAX_NS; ++want) {
+        int L = (p.cap + want - 1) / want;
+        L = (L + half - 1) / half * half;
+        if (p.paged) L = (L + p.page - 1) / p.page * p.page;
+        const int ns = (p.cap + L - 1) / L;
+        if (ns > PS_MAX_NS) continue;
+        const long long per_cta = ((long long)units0 * ns + num_sms - 1) / num_sms;
+        const long long cost = per_cta * L + 16LL * ns;
+        if (best < 0 || cost < best) {
+            best = cost;
+            bl = L;
+            bn = ns;
+        }
+    }
+    p.split_len = bl;
+    p.nsplit = bn;
+    plan->grid = num_sms;
+    plan->block = PS_THREADS;
+    plan->smem = (size_t)PS_S * PS_SLOT + 1024;
+    plan->fn = fn;
+    int dev = 0, optin = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess) return e;
+    cudaFuncAttributes fa;
+    if ((e = cudaFuncGetAttributes(&fa, fn)) != cudaSuccess) return e;
+    if (plan->smem + fa.sharedSizeBytes > (size_t)optin) return cudaErrorNotSupported;
+    if ((e = raise_smem_cap(fn)) != cudaSuccess) return e;
+    int occ = 0;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, PS_THREADS, plan->smem)) != cudaSuccess) return e;
+    if (occ < 1) return cudaErrorNotSupported;
+    return cudaSuccess;
+}
+
+size_t persist_tmap_bytes(int n_layers) { return (size_t)n_layers * 4 * sizeof(CUtensorMap); }
+
+typedef CUresult (*PsEncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                               const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                               CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// host images of the tensor maps [layer][K|V][full box | half box (or page box)]
+cudaError_t persist_tmaps(const PersistParams& p, void* const* kv, void* host_out) {
+    void* fptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fptr, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return cudaErrorNotSupported;
+    PsEncodeFn fn = reinterpret_cast<PsEncodeFn>(fptr);
+    CUtensorMap* out = static_cast<CUtensorMap*>(host_out);
+    const int pps = PS_SLOT / (2 * p.hd * 2);
+    const long long rows = p.paged ? (long long)p.num_pages * p.Hkv * p.page : (long long)p.R * p.Hkv * p.cap;
+    for (int l = 0; l < p.L; ++l)
+        for (int w = 0; w < 2; ++w)
+            for (int b = 0; b < 2; ++b) {
+                const int box_rows = p.paged ? p.page : (b == 0 ? pps : pps / 2);
+                cuuint64_t dims[2] = {(cuuint64_t)p.hd, (cuuint64_t)rows};
+                cuuint64_t strides[1] = {(cuuint64_t)p.hd * 2};
+                cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+                cuuint32_t estr[2] = {1u, 1u};
+                CUresult r = fn(&out[(l * 2 + w) * 2 + b], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv[2 * l + w], dims,
+                                strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+            }
+    return cudaSuccess;
+}
+
+cudaError_t persist_launch(const PersistPlan& plan, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(plan.grid);
+    cfg.blockDim = dim3(plan.block);
+    cfg.dynamicSmemBytes = plan.smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;   // every CTA resident: grid-wide waits always end
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void* args[] = {const_cast<PersistParams*>(&plan.p)};
+    return cudaLaunchKernelExC(&cfg, plan.fn, args);
+}
+
+}  // namespace gd

@@ -53,7 +53,7 @@ class Decoder:
 
     def __init__(self, cfg: B.dec_config, weights: dict, cap: int, rows: int = 1, kv_layout: str = "contiguous",
                  page_size: int = 16, num_pages: int = 0, stream: Optional[torch.cuda.Stream] = None,
-                 lib_workspace: bool = False):
+                 lib_workspace: bool = False, strategy: str = "graph"):
         self.cfg = cfg
         self.rows, self.cap = rows, cap
         self.layout = B.DEC_KV_PAGED if kv_layout == "paged" else B.DEC_KV_CONTIGUOUS
@@ -63,6 +63,7 @@ class Decoder:
         self._weights = weights   # borrowed device memory must outlive the handle
         try:
             B.dec_load_weights(self.h, self._bindings(weights))
+            B.dec_set_strategy(self.h, B.DEC_STRATEGY_PERSISTENT if strategy == "persistent" else B.DEC_STRATEGY_GRAPH)
             self.ws = None
             ws_ptr, ws_bytes = None, 0
             if not lib_workspace:

@@ -79,6 +79,22 @@ typedef enum dec_dtype { DEC_DTYPE_F32 = 0, DEC_DTYPE_BF16 = 1 } dec_dtype;
  *               (a ScatterUpdate through Slot::WriteMap). */
 typedef enum dec_kv_layout { DEC_KV_CONTIGUOUS = 0, DEC_KV_PAGED = 1 } dec_kv_layout;
 
+/* How the captured step executes (chosen before dec_capture):
+ *   GRAPH       the pages' strategy: the step's dispatch sequence (embedding,
+ *               5 fused kernels per layer, head) recorded into one CUDA graph
+ *               with programmatic dependent launches ("Execution", "Per
+ *               backend", PTX row);
+ *   PERSISTENT  the step as one cooperative kernel captured as the graph's
+ *               single node; phases separated by grid-wide dependency counters
+ *               and one continuous weight/KV stream per SM (the pages' possible
+ *               future megakernel strategy).  Same arithmetic, other fp32
+ *               summation order: results agree with GRAPH within the parity
+ *               tolerances, not bit for bit; replay and eager runs of one
+ *               strategy are bit-identical.  Available for bf16 weights and
+ *               KV, rows = 1 and the 8B-shape / 1B-class layer shapes
+ *               (DEC_E_UNSUPPORTED at capture otherwise). */
+typedef enum dec_strategy { DEC_STRATEGY_GRAPH = 0, DEC_STRATEGY_PERSISTENT = 1 } dec_strategy;
+
 /* Model configuration.  RMSNorm is x / sqrt(mean(x^2) + rms_eps) * g; RoPE is
  * the half-split rotation of pairs (i, i + head_dim/2) by pos * rope_theta^(-2i/head_dim);
  * attention scale is 1/sqrt(head_dim); q head i reads kv head i / (n_heads / n_kv_heads). */
@@ -140,6 +156,8 @@ typedef struct dec_stats {
     int32_t rows;
     int32_t cap;
     int32_t kv_layout;
+    int32_t strategy;         /* dec_strategy of the capture */
+    int32_t reserved;
     double last_step_us;      /* host wall time of the last dec_step */
     int64_t workspace_bytes;  /* device bytes the capture uses (KV included) */
     int64_t kv_bytes;         /* device bytes of K and V over all layers */
@@ -213,6 +231,10 @@ int dec_launch(dec_handle *h, const int32_t *dev_slots);
  * step's results back; any pointer may be NULL.  Returns DEC_E_DEVICE_FAULT if
  * the last step's error word is non-zero. */
 int dec_wait(dec_handle *h, float *logits_out, int32_t *ids_out, uint8_t *nonfinite_out);
+
+/* Choose the execution strategy (dec_strategy) for the coming dec_capture;
+ * DEC_E_STATE after capture.  Default DEC_STRATEGY_GRAPH. */
+int dec_set_strategy(dec_handle *h, int32_t strategy);
 
 /* 1: later steps launch the recorded kernel sequence directly on the stream
  * instead of replaying the graph (same kernels, same arguments); 0: replay. */

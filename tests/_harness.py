@@ -90,3 +90,102 @@ def assert_greedy(gpu_id, ref_logits, what=""):
 
 def kv_as_float(a: np.ndarray) -> np.ndarray:
     return gen.bf16_bits_to_f32(a) if a.dtype == np.uint16 else a
+
+
+# ---- shared GPU cases (called by the parity tests of each step strategy) ----
+
+def run_sequence(wl, n_prompt, n_decode, mw=None, check_kv=True, **kw):
+    """Prompt stepped token by token, then greedy decode fed with the oracle's pick."""
+    from gen.device import read_kv
+    dec, mw = make_decoder(wl, mw, **kw)
+    orc = oracle.Oracle(mw, cap=wl.cap)
+    toks = list(gen.prompt_tokens(wl, n=n_prompt))
+    strict = 0
+    pos = 0
+    for i in range(n_prompt + n_decode):
+        t = toks[i]
+        res = dec.step([t], [pos])
+        ref = orc.step(0, t, pos)
+        assert_close(res.logits[0], ref, wl, f"{wl.name} step {i} pos {pos}")
+        assert res.nonfinite[0] == 0
+        assert int(res.ids[0]) == int(np.argmax(res.logits[0]))   # device argmax = argmax of its logits
+        strict += assert_greedy(res.ids[0], ref, f"{wl.name} step {i}")
+        if i + 1 >= n_prompt:
+            toks.append(oracle.argmax(ref))
+        pos += 1
+    if check_kv:
+        n = pos
+        for l in range(wl.n_layers):
+            for which, store in ((0, orc.K[0][l]), (1, orc.V[0][l])):
+                got = kv_as_float(read_kv(dec.kv(l, which), 0, n))
+                assert_close_state(got, kv_as_float(store[:n]), wl, f"{wl.name} KV layer {l} which {which}")
+    st = dec.stats()
+    dec.close()
+    return strict, st
+
+
+def prefill_both(dec, orc, wl, row, npos, slot_map=None):
+    from gen.device import place_kv
+    for l in range(wl.n_layers):
+        for which in (0, 1):
+            blk = gen.kv_prefill(wl, l, which, row, npos)
+            place_kv(dec.kv(l, which), blk, row, 0, slot_map, wl.page_size)
+            store = orc.K[0][l] if which == 0 else orc.V[0][l]
+            store[:npos] = blk
+
+
+def prefilled_positions_case(wl, **kw):
+    """One step at each of wl.positions over KV pre-filled N(0,1) below pos: logits,
+    greedy id and the K write at pos against the oracle, the prefill untouched."""
+    dec, mw = make_decoder(wl, **kw)
+    orc = oracle.Oracle(mw, cap=wl.cap)
+    tok = int(gen.prompt_tokens(wl, n=1)[0])
+    for pos in wl.positions:
+        dec.reset_state()
+        for l in range(wl.n_layers):
+            orc.K[0][l][:] = 0
+            orc.V[0][l][:] = 0
+        prefill_both(dec, orc, wl, 0, pos)
+        res = dec.step([tok], [pos])
+        ref = orc.step(0, tok, pos)
+        assert_close(res.logits[0], ref, wl, f"{wl.name} pos {pos}")
+        assert_greedy(res.ids[0], ref, f"{wl.name} pos {pos}")
+        from gen.device import read_kv
+        for l in (0, wl.n_layers // 2, wl.n_layers - 1):
+            got = kv_as_float(read_kv(dec.kv(l, 0), 0, pos + 1))
+            assert_close_state(got[pos], kv_as_float(orc.K[0][l][pos]), wl, f"{wl.name} K write layer {l}")
+            assert np.array_equal(got[:pos], kv_as_float(orc.K[0][l][:pos]))   # prefill untouched
+    dec.close()
+
+
+def paged_case(base: str, rows: int, n_steps: int, n_layers=None, **kw):
+    """Paged KV through a seeded random page table, rows at independent positions,
+    compared with the oracle row by row; the KV write lands only at WriteMap."""
+    import torch
+    wl = gen.WORKLOADS[base]
+    shape = dict(name=f"{base}_paged{rows}", rows=rows, layout="paged", page_size=16,
+                 num_pages=rows * wl.cap // 16 + 7)
+    if n_layers:
+        shape["n_layers"] = n_layers
+    wl = wl.replace(**shape)
+    dec, mw = make_decoder(wl, **kw)
+    sm = gen.permutation(wl.seed, 99, wl.num_pages)[: rows * (wl.cap // 16)].reshape(rows, wl.cap // 16)
+    dec.set_slot_map(sm)
+    orcs = [oracle.Oracle(mw, cap=wl.cap) for _ in range(rows)]
+    start = [int(x) for x in gen.ints(wl.seed, 98, 0, wl.cap - n_steps, rows)]
+    toks = [gen.prompt_tokens(wl, row=r, n=n_steps) for r in range(rows)]
+    for i in range(n_steps):
+        pos = [start[r] + i for r in range(rows)]
+        before = [dec.kv(l, 0).clone() for l in range(wl.n_layers)]
+        res = dec.step([toks[r][i] for r in range(rows)], pos)
+        wmap = [int(sm[r][p // 16]) * 16 + p % 16 for r, p in enumerate(pos)]
+        for l in range(wl.n_layers):
+            diff = (dec.kv(l, 0) != before[l]).any(dim=3).any(dim=1)   # [pages, page]
+            got = sorted((int(a) * 16 + int(b)) for a, b in torch.nonzero(diff).tolist())
+            assert got == sorted(wmap), (l, got, wmap)
+        for r in range(rows):
+            # the oracle sees only positions the step wrote: zeros before start (same as the GPU pool)
+            ref = orcs[r].step(0, int(toks[r][i]), pos[r])
+            assert_close(res.logits[r], ref, wl, f"{wl.name} row {r} step {i}")
+            assert_greedy(res.ids[r], ref)
+    dec.close()

@@ -11,45 +11,16 @@ import pytest
 
 import gen
 import oracle
-from _harness import assert_close, assert_close_state, assert_greedy, kv_as_float, make_decoder
+from _harness import (assert_close, assert_close_state, assert_greedy, kv_as_float, make_decoder, paged_case,
+                      prefilled_positions_case, run_sequence)
 
 pytestmark = pytest.mark.gpu
-
-
-def _run_sequence(wl, n_prompt, n_decode, mw=None, check_kv=True, rows=None):
-    """Prompt stepped token by token, then greedy decode fed with the oracle's pick."""
-    from gen.device import read_kv
-    dec, mw = make_decoder(wl, mw)
-    orc = oracle.Oracle(mw, cap=wl.cap)
-    toks = list(gen.prompt_tokens(wl, n=n_prompt))
-    strict = 0
-    pos = 0
-    for i in range(n_prompt + n_decode):
-        t = toks[i]
-        res = dec.step([t], [pos])
-        ref = orc.step(0, t, pos)
-        assert_close(res.logits[0], ref, wl, f"{wl.name} step {i} pos {pos}")
-        assert res.nonfinite[0] == 0
-        assert int(res.ids[0]) == int(np.argmax(res.logits[0]))   # device argmax = argmax of its logits
-        strict += assert_greedy(res.ids[0], ref, f"{wl.name} step {i}")
-        if i + 1 >= n_prompt:
-            toks.append(oracle.argmax(ref))
-        pos += 1
-    if check_kv:
-        n = pos
-        for l in range(wl.n_layers):
-            for which, store in ((0, orc.K[0][l]), (1, orc.V[0][l])):
-                got = kv_as_float(read_kv(dec.kv(l, which), 0, n))
-                assert_close_state(got, kv_as_float(store[:n]), wl, f"{wl.name} KV layer {l} which {which}")
-    st = dec.stats()
-    dec.close()
-    return strict, st
 
 
 @pytest.mark.parametrize("name", ["tiny", "tiny_gain"])
 def test_tiny_prompt_then_greedy(name):
     wl = gen.WORKLOADS[name]
-    strict, st = _run_sequence(wl, wl.prompt_len, wl.decode_steps)
+    strict, st = run_sequence(wl, wl.prompt_len, wl.decode_steps)
     assert st["replays"] == wl.prompt_len + wl.decode_steps
     assert st["graph_nodes"] == st["kernels_per_step"]
 
@@ -57,18 +28,18 @@ def test_tiny_prompt_then_greedy(name):
 @pytest.mark.parametrize("kv_heads", [1, 2])
 def test_tiny_gqa_groups(kv_heads):
     wl = gen.WORKLOADS["tiny"].replace(name=f"tiny_kv{kv_heads}", n_kv_heads=kv_heads)
-    _run_sequence(wl, 16, 8)
+    run_sequence(wl, 16, 8)
 
 
 def test_tiny_bf16_weights_and_kv():
     wl = gen.WORKLOADS["tiny"].replace(name="tiny_bf16", wdtype="bf16", kvdtype="bf16")
-    _run_sequence(wl, 16, 16)
+    run_sequence(wl, 16, 16)
 
 
 def test_1b_prompt_then_greedy():
     # configuration 2: 128 prompt tokens stepped in, then 256 greedy decode steps
     wl = gen.WORKLOADS["1b"]
-    strict, st = _run_sequence(wl, wl.prompt_len, wl.decode_steps)
+    strict, st = run_sequence(wl, wl.prompt_len, wl.decode_steps)
     assert strict > 0
 
 
@@ -140,39 +111,10 @@ def test_kv_write_touches_only_pos():
     dec.close()
 
 
-def _prefill_both(dec, orc, wl, row, npos, slot_map=None):
-    from gen.device import place_kv
-    for l in range(wl.n_layers):
-        for which in (0, 1):
-            blk = gen.kv_prefill(wl, l, which, row, npos)
-            place_kv(dec.kv(l, which), blk, row, 0, slot_map, wl.page_size)
-            store = orc.K[0][l] if which == 0 else orc.V[0][l]
-            store[:npos] = blk
-
-
 @pytest.mark.slow
 def test_8b_decode_at_prefilled_positions():
     # configuration 3 at full size: one step at pos in {1, 1024, 4096, 8191} over KV pre-filled N(0,1)
-    wl = gen.WORKLOADS["8b"]
-    dec, mw = make_decoder(wl)
-    orc = oracle.Oracle(mw, cap=wl.cap)
-    tok = int(gen.prompt_tokens(wl, n=1)[0])
-    for pos in wl.positions:
-        dec.reset_state()
-        for l in range(wl.n_layers):
-            orc.K[0][l][:] = 0
-            orc.V[0][l][:] = 0
-        _prefill_both(dec, orc, wl, 0, pos)
-        res = dec.step([tok], [pos])
-        ref = orc.step(0, tok, pos)
-        assert_close(res.logits[0], ref, wl, f"8b pos {pos}")
-        assert_greedy(res.ids[0], ref, f"8b pos {pos}")
-        from gen.device import read_kv
-        for l in (0, wl.n_layers // 2, wl.n_layers - 1):
-            got = kv_as_float(read_kv(dec.kv(l, 0), 0, pos + 1))
-            assert_close_state(got[pos], kv_as_float(orc.K[0][l][pos]), wl, f"8b K write layer {l}")
-            assert np.array_equal(got[:pos], kv_as_float(orc.K[0][l][:pos]))   # prefill untouched
-    dec.close()
+    prefilled_positions_case(gen.WORKLOADS["8b"])
 
 
 @pytest.mark.slow
@@ -200,45 +142,12 @@ def test_1b_long_cap_rows4():
     dec.close()
 
 
-def _paged_case(base: str, rows: int, n_steps: int, n_layers=None):
-    """Paged KV through a seeded random page table, rows at independent positions,
-    compared with the oracle row by row; the KV write lands only at WriteMap."""
-    import torch
-    wl = gen.WORKLOADS[base]
-    kw = dict(name=f"{base}_paged{rows}", rows=rows, layout="paged", page_size=16,
-              num_pages=rows * wl.cap // 16 + 7)
-    if n_layers:
-        kw["n_layers"] = n_layers
-    wl = wl.replace(**kw)
-    dec, mw = make_decoder(wl)
-    sm = gen.permutation(wl.seed, 99, wl.num_pages)[: rows * (wl.cap // 16)].reshape(rows, wl.cap // 16)
-    dec.set_slot_map(sm)
-    orcs = [oracle.Oracle(mw, cap=wl.cap) for _ in range(rows)]
-    start = [int(x) for x in gen.ints(wl.seed, 98, 0, wl.cap - n_steps, rows)]
-    toks = [gen.prompt_tokens(wl, row=r, n=n_steps) for r in range(rows)]
-    for i in range(n_steps):
-        pos = [start[r] + i for r in range(rows)]
-        before = [dec.kv(l, 0).clone() for l in range(wl.n_layers)]
-        res = dec.step([toks[r][i] for r in range(rows)], pos)
-        wmap = [int(sm[r][p // 16]) * 16 + p % 16 for r, p in enumerate(pos)]
-        for l in range(wl.n_layers):
-            diff = (dec.kv(l, 0) != before[l]).any(dim=3).any(dim=1)   # [pages, page]
-            got = sorted((int(a) * 16 + int(b)) for a, b in torch.nonzero(diff).tolist())
-            assert got == sorted(wmap), (l, got, wmap)
-        for r in range(rows):
-            # the oracle sees only positions the step wrote: zeros before start (same as the GPU pool)
-            ref = orcs[r].step(0, int(toks[r][i]), pos[r])
-            assert_close(res.logits[r], ref, wl, f"{wl.name} row {r} step {i}")
-            assert_greedy(res.ids[r], ref)
-    dec.close()
-
-
 def test_paged_tiny_rows2():
-    _paged_case("tiny", 2, 12)
+    paged_case("tiny", 2, 12)
 
 
 def test_paged_1b_rows4():
-    _paged_case("1b", 4, 6, n_layers=4)
+    paged_case("1b", 4, 6, n_layers=4)
 
 
 @pytest.mark.parametrize("name, rows", [("1b", 2), ("8b", 1)])
