@@ -124,6 +124,19 @@ def _traffic_from_profile():
     return float(m.group(1))
 
 
+def _workload(args):
+    import gen
+    wl = gen.WORKLOADS[args.workload]
+    over = {}
+    if args.layers:
+        over["n_layers"] = args.layers
+    if args.vocab:
+        over["vocab"] = args.vocab
+    if over:   # a reduced copy of the workload, for profiler captures only
+        wl = wl.replace(name=f"{wl.name}_reduced", **over)
+    return wl
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
 
@@ -134,7 +147,7 @@ def run_ours(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     dev = f"cuda:{local_rank}"
-    wl = gen.WORKLOADS[args.workload]
+    wl = _workload(args)
     # weights: drawn from the seeded generator tensor by tensor, uploaded, host copy dropped
     w = {"layers": []}
     mw = gen.make_weights(wl) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
@@ -313,7 +326,7 @@ def cpu_baseline(wl, mw, plist, toks, seconds=20.0, steps_cap=None):
 
 def run_reference(args):
     import gen
-    wl = gen.WORKLOADS[args.workload]
+    wl = _workload(args)
     mw = gen.make_weights(wl)
     plist = _positions(wl)
     toks = gen.ints(wl.seed, 0x51, 0, wl.vocab, wl.rows * len(plist)).reshape(len(plist), wl.rows)
@@ -340,6 +353,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--strategy", default="graph", choices=["graph", "persistent"],
                     help="graph: the step's kernel sequence in one CUDA graph; persistent: one whole-step kernel")
+    ap.add_argument("--layers", type=int, default=0, help="override the layer count (reduced case for profilers)")
+    ap.add_argument("--vocab", type=int, default=0, help="override the vocabulary (reduced case for profilers)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

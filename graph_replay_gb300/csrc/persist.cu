@@ -37,14 +37,19 @@
 
 namespace gd {
 
-constexpr int PS_WARPS = 16;
-constexpr int PS_THREADS = PS_WARPS * 32;
-constexpr int PS_SL = 8;                   // K-slices
-constexpr int PS_GR = 2;                   // row groups (alternate rows of a stage)
-constexpr int PS_SLOT = 65536;             // bytes per ring slot
-constexpr int PS_S = 3;                    // ring slots
+constexpr int PS_CW = 8;                   // compute warps
+constexpr int PS_CT = PS_CW * 32;          // compute threads
+constexpr int PS_THREADS = PS_CT + 32;     // + one producer warp
+constexpr int PS_SL = PS_CW;               // K-slices of a GEMV stage, one per compute warp
+constexpr int PS_CBAR = 1;                 // named barrier of the compute warps
+#ifndef PS_SLOT_KB
+#define PS_SLOT_KB 64
+#endif
+constexpr int PS_SLOT = PS_SLOT_KB * 1024;  // bytes per ring slot
+constexpr int PS_S = 196608 / PS_SLOT;      // ring slots (192 KB of shared memory)
 constexpr int PS_MAX_RPS = 32;
 constexpr int PS_MAX_RES = 64;
+constexpr int PS_RED_ROWS = 192;          // rows whose slice partials wait in shared memory
 constexpr int PS_AW = 4;                   // warps that compute attention
 constexpr int PS_MAX_L = 64;               // layers whose weight pointers fit the smem table
 constexpr int PS_MAX_NS = 64;              // attention splits per (row, kv head)
@@ -59,13 +64,38 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
     return v;
 }
 
+// The producer's position in the CTA's whole-step stream of ring stages (in
+// the producer thread's registers).  GEMV phases: the CTA's rows are up to
+// three byte runs, one per stacked weight segment; a stage takes the next
+// stage_bytes of them.
+struct PsCursor {
+    int p, loc, nst;           // phase, stage within the phase, stages of the phase (-1: not set up)
+    int kind, layer;
+    const unsigned char* src;  // next byte of the current run
+    uint32_t run_left, stage_bytes, phase_left;
+    int run, nruns;
+    const unsigned char *rs0, *rs1, *rs2;
+    uint32_t rb0, rb1, rb2;
+    int u, uloc, ust;          // attention: unit, stage within the unit, the unit's stages
+};
+
+// One stage, resolved before its ring slot is free: a GEMV stage is up to three
+// bulk copies; an attention stage is issued from (layer, unit, stage in unit).
+struct PsStage {
+    int kind;
+    int layer, u, uloc;
+    const unsigned char *s0, *s1, *s2;
+    uint32_t b0, b1, b2;
+};
+
 struct PsShared {
-    uint64_t full_bar[PS_S];
+    uint64_t full_bar[PS_S];   // a ring slot's copy landed (producer's expect_tx + the copy bytes)
+    uint64_t empty_bar[PS_S];  // every compute warp is done with the slot
     int abort;
     int last;
     const void* wtab[PS_MAX_L * 9];
-    float red[2][PS_MAX_RPS][PS_SL];
-    float nrm[PS_WARPS];
+    float red[PS_RED_ROWS][PS_SL];
+    float nrm[PS_CW];
     float res[PS_MAX_RES];
     float wm[PS_AW][8], wl[PS_AW][8];
     float cm[8 * PS_MAX_NS], cw[8 * PS_MAX_NS];
@@ -85,16 +115,13 @@ struct PsState {
     unsigned char* ring;
     int cta, nc, np, tid;
     int cons;   // stages consumed (uniform over the CTA)
-    // issue cursor, thread 0 only
-    int iss_p, iss_loc, iss_tot, iss_nst;
 
     static constexpr int PPS = PS_SLOT / (2 * HD * 2);   // keys per full attention stage
     static constexpr int TILE = PPS * HD * 2;            // bytes of the K (or V) tile
     static constexpr int SUB = HD / 64;
 
     __device__ PsState(const PersistParams& p, PsShared& s, unsigned char* r)
-        : P(p), sh(s), ring(r), cta(blockIdx.x), nc(gridDim.x), np(5 * p.L + 2), tid(threadIdx.x), cons(0),
-          iss_p(0), iss_loc(0), iss_tot(0), iss_nst(-1) {}
+        : P(p), sh(s), ring(r), cta(blockIdx.x), nc(gridDim.x), np(5 * p.L + 2), tid(threadIdx.x), cons(0) {}
 
     __device__ int kind(int p) const { return p == 0 ? PK_EMBED : (p == np - 1 ? PK_HEAD : 1 + (p - 1) % 5); }
     __device__ int layer(int p) const { return (p - 1) / 5; }
@@ -118,108 +145,151 @@ struct PsState {
         g.N = g.n[0] + g.n[1] + g.n[2];
     }
     __device__ int units() const { return P.R * P.Hkv * P.nsplit; }
-    __device__ int unit_len(int u) const {
-        const int s = u % P.nsplit;
-        const int j0 = s * P.split_len;
-        return min(j0 + P.split_len, P.cap) - j0;
-    }
-    __device__ int unit_stages(int u) const { return (unit_len(u) + PPS - 1) / PPS; }
-    __device__ int stages(int p) const {
-        const int k = kind(p);
-        if (k == PK_EMBED) return 0;
-        if (k == PK_ATTN) {
-            int n = 0;
-            for (int u = cta; u < units(); u += nc) n += unit_stages(u);
-            return n;
-        }
-        GvGeom g;
-        geom(k, k == PK_HEAD ? 0 : layer(p), g);
-        int r0, r1;
-        rows_of(g.N, r0, r1);
-        return (r1 - r0 + g.rps - 1) / g.rps;
+    __device__ int unit_stages(int u) const {
+        const int j0 = (u % P.nsplit) * P.split_len;
+        return (min(j0 + P.split_len, P.cap) - j0 + PPS - 1) / PPS;
     }
 
     __device__ const CUtensorMap* tmap(int l, int which, int box) const {
         return reinterpret_cast<const CUtensorMap*>(P.tmaps) + (l * 2 + which) * 2 + box;
     }
 
-    // thread 0: issue the next stage of the CTA's whole-step stream
-    __device__ void issue_next() {
-        while (iss_p < np) {
-            if (iss_nst < 0) iss_nst = stages(iss_p);
-            if (iss_loc < iss_nst) break;
-            ++iss_p;
-            iss_loc = 0;
-            iss_nst = -1;
+    // ---- the stream of stages (producer warp, lane 0) ----
+    __device__ void setup(PsCursor& c) const {
+        c.kind = kind(c.p);
+        c.layer = (c.kind == PK_EMBED || c.kind == PK_HEAD) ? 0 : layer(c.p);
+        if (c.kind == PK_EMBED) {
+            c.nst = 0;
+        } else if (c.kind == PK_ATTN) {
+            int n = 0;
+            for (int u = cta; u < units(); u += nc) n += unit_stages(u);
+            c.nst = n;
+            c.u = cta;
+            c.uloc = 0;
+            c.ust = cta < units() ? unit_stages(cta) : 0;
+        } else {
+            GvGeom g;
+            geom(c.kind, c.layer, g);
+            int r0, r1;
+            rows_of(g.N, r0, r1);
+            const uint32_t rb = (uint32_t)g.K * 2u;
+            // the CTA's rows [r0, r1) cut by the segments [0, n0), [n0, n0 + n1), [n0 + n1, N)
+            const int e0 = g.n[0], e1 = g.n[0] + g.n[1];
+            const int a0 = r0, z0 = min(r1, e0);
+            const int a1 = max(r0, e0), z1 = min(r1, e1);
+            const int a2 = max(r0, e1), z2 = r1;
+            const unsigned char* w0 = static_cast<const unsigned char*>(g.w[0]);
+            const unsigned char* w1 = static_cast<const unsigned char*>(g.w[1]);
+            const unsigned char* w2 = static_cast<const unsigned char*>(g.w[2]);
+            const unsigned char* q0 = w0 + (size_t)a0 * rb;
+            const unsigned char* q1 = w1 + (size_t)(a1 - e0) * rb;
+            const unsigned char* q2 = w2 + (size_t)(a2 - e1) * rb;
+            const uint32_t n0 = z0 > a0 ? (uint32_t)(z0 - a0) * rb : 0u;
+            const uint32_t n1 = z1 > a1 ? (uint32_t)(z1 - a1) * rb : 0u;
+            const uint32_t n2 = z2 > a2 ? (uint32_t)(z2 - a2) * rb : 0u;
+            // non-empty runs, in order
+            c.rs0 = n0 ? q0 : (n1 ? q1 : q2);
+            c.rb0 = n0 ? n0 : (n1 ? n1 : n2);
+            c.rs1 = n0 ? (n1 ? q1 : q2) : q2;
+            c.rb1 = n0 ? (n1 ? n1 : n2) : (n1 ? n2 : 0u);
+            c.rs2 = q2;
+            c.rb2 = (n0 && n1) ? n2 : 0u;
+            c.nruns = (n0 != 0u) + (n1 != 0u) + (n2 != 0u);
+            c.run = 0;
+            c.src = c.rs0;
+            c.run_left = c.rb0;
+            c.stage_bytes = (uint32_t)g.rps * rb;
+            c.phase_left = (uint32_t)(r1 - r0) * rb;
+            c.nst = (r1 - r0 + g.rps - 1) / g.rps;
         }
-        if (iss_p >= np) return;
-        const int slot = iss_tot % PS_S;
-        uint64_t* bar = &sh.full_bar[slot];
-        unsigned char* dst = ring + (size_t)slot * PS_SLOT;
-        const int k = kind(iss_p);
-        if (k == PK_ATTN) {
-            const int l = layer(iss_p);
-            int loc = iss_loc, u = cta;
-            while (loc >= unit_stages(u)) {
-                loc -= unit_stages(u);
-                u += nc;
+    }
+    // take up to `want` bytes from the runs (the current one, then the next)
+    __device__ static uint32_t take(PsCursor& c, uint32_t want, const unsigned char*& src) {
+        if (c.run_left == 0u && c.run + 1 < c.nruns) {
+            ++c.run;
+            c.src = c.run == 1 ? c.rs1 : c.rs2;
+            c.run_left = c.run == 1 ? c.rb1 : c.rb2;
+        }
+        const uint32_t n = min(want, c.run_left);
+        src = c.src;
+        c.src += n;
+        c.run_left -= n;
+        return n;
+    }
+    // resolve the next stage of the stream into s and step past it; false at the end
+    __device__ bool next(PsCursor& c, PsStage& s) const {
+        for (;;) {
+            if (c.p >= np) return false;
+            if (c.nst < 0) setup(c);
+            if (c.loc < c.nst) break;
+            ++c.p;
+            c.loc = 0;
+            c.nst = -1;
+        }
+        s.kind = c.kind;
+        if (c.kind == PK_ATTN) {
+            s.layer = c.layer;
+            s.u = c.u;
+            s.uloc = c.uloc;
+            if (++c.uloc == c.ust) {
+                c.u += nc;
+                c.uloc = 0;
+                c.ust = c.u < units() ? unit_stages(c.u) : 0;
             }
-            const int s = u % P.nsplit, g = (u / P.nsplit) % P.Hkv, r = u / (P.nsplit * P.Hkv);
-            const int j0 = s * P.split_len;
-            const int j1 = min(j0 + P.split_len, P.cap);
-            const int p0 = j0 + loc * PPS, p1 = min(p0 + PPS, j1);
-            const int n = p1 - p0;
-            unsigned char* kd = dst;
-            unsigned char* vd = dst + TILE;
-            mbar_arrive_expect_tx(bar, (uint32_t)(2 * n * HD * 2));
-            if (PAGED) {
-                const int pg_size = P.page;
-                for (int q = p0; q < p1; q += pg_size) {
-                    int pg = P.slot_map[(size_t)r * P.pages_per_row + q / pg_size];
-                    if (pg < 0 || pg >= P.num_pages) pg = 0;   // flagged by the consumers
-                    const int y = (pg * P.Hkv + g) * pg_size;
-#pragma unroll
-                    for (int sb = 0; sb < SUB; ++sb) {
-                        tma_load_2d(kd + sb * PPS * 128 + (q - p0) * 128, tmap(l, 0, 0), sb * 64, y, bar);
-                        tma_load_2d(vd + sb * PPS * 128 + (q - p0) * 128, tmap(l, 1, 0), sb * 64, y, bar);
-                    }
-                }
-            } else {
-                const int y = (r * P.Hkv + g) * P.cap + p0;
-                const int box = n == PPS ? 0 : 1;   // full stage, or the half stage that ends a split
+        } else {
+            const uint32_t total = min(c.stage_bytes, c.phase_left);
+            s.b0 = take(c, total, s.s0);
+            s.b1 = take(c, total - s.b0, s.s1);
+            s.b2 = take(c, total - s.b0 - s.b1, s.s2);
+            c.phase_left -= total;
+        }
+        ++c.loc;
+        return true;
+    }
+    // copy stage s into ring slot `slot`
+    __device__ void issue(const PsStage& s, int slot) const {
+        unsigned char* dst = ring + (size_t)slot * PS_SLOT;
+        uint64_t* bar = &sh.full_bar[slot];
+        if (s.kind != PK_ATTN) {
+            mbar_arrive_expect_tx(bar, s.b0 + s.b1 + s.b2);
+            if (s.b0) bulk_g2s(dst, s.s0, s.b0, bar);
+            if (s.b1) bulk_g2s(dst + s.b0, s.s1, s.b1, bar);
+            if (s.b2) bulk_g2s(dst + s.b0 + s.b1, s.s2, s.b2, bar);
+            return;
+        }
+        const int l = s.layer, u = s.u;
+        const int sp = u % P.nsplit, g = (u / P.nsplit) % P.Hkv, r = u / (P.nsplit * P.Hkv);
+        const int j0 = sp * P.split_len;
+        const int j1 = min(j0 + P.split_len, P.cap);
+        const int p0 = j0 + s.uloc * PPS, p1 = min(p0 + PPS, j1);
+        const int n = p1 - p0;
+        unsigned char* kd = dst;
+        unsigned char* vd = dst + TILE;
+        mbar_arrive_expect_tx(bar, (uint32_t)(2 * n * HD * 2));
+        if (PAGED) {
+            const int pg_size = P.page;
+            for (int q = p0; q < p1; q += pg_size) {
+                int pg = P.slot_map[(size_t)r * P.pages_per_row + q / pg_size];
+                if (pg < 0 || pg >= P.num_pages) pg = 0;   // flagged by the consumers
+                const int y = (pg * P.Hkv + g) * pg_size;
 #pragma unroll
                 for (int sb = 0; sb < SUB; ++sb) {
-                    tma_load_2d(kd + sb * PPS * 128, tmap(l, 0, box), sb * 64, y, bar);
-                    tma_load_2d(vd + sb * PPS * 128, tmap(l, 1, box), sb * 64, y, bar);
+                    tma_load_2d(kd + sb * PPS * 128 + (q - p0) * 128, tmap(l, 0, 0), sb * 64, y, bar);
+                    tma_load_2d(vd + sb * PPS * 128 + (q - p0) * 128, tmap(l, 1, 0), sb * 64, y, bar);
                 }
             }
         } else {
-            GvGeom gg;
-            geom(k, k == PK_HEAD ? 0 : layer(iss_p), gg);
-            int r0, r1;
-            rows_of(gg.N, r0, r1);
-            const int a = r0 + iss_loc * gg.rps, b = min(a + gg.rps, r1);
-            const size_t rb = (size_t)gg.K * 2;
-            mbar_arrive_expect_tx(bar, (uint32_t)((size_t)(b - a) * rb));
-            int row = a;
-            while (row < b) {
-                int base = 0, sg = 0;
-                while (sg < 2 && row >= base + gg.n[sg]) {
-                    base += gg.n[sg];
-                    ++sg;
-                }
-                const int e = min(b, base + gg.n[sg]);
-                const uint32_t bytes = (uint32_t)((size_t)(e - row) * rb);
-                bulk_g2s(dst, reinterpret_cast<const unsigned char*>(gg.w[sg]) + (size_t)(row - base) * rb, bytes, bar);
-                dst += bytes;
-                row = e;
+            const int y = (r * P.Hkv + g) * P.cap + p0;
+            const int box = n == PPS ? 0 : 1;   // full stage, or the half stage that ends a split
+#pragma unroll
+            for (int sb = 0; sb < SUB; ++sb) {
+                tma_load_2d(kd + sb * PPS * 128, tmap(l, 0, box), sb * 64, y, bar);
+                tma_load_2d(vd + sb * PPS * 128, tmap(l, 1, box), sb * 64, y, bar);
             }
         }
-        ++iss_loc;
-        ++iss_tot;
     }
 
-    // consumer side of one stage: wait for it; false after an abort
+    // consumer side of one stage: wait for it (skipped after an abort)
     __device__ const unsigned char* stage_wait() {
         const int slot = cons % PS_S;
         volatile int* ab = &sh.abort;
@@ -229,18 +299,43 @@ struct PsState {
         }
         return ring + (size_t)slot * PS_SLOT;
     }
-    // every thread is done with the stage: thread 0 refills the slot
+    // this warp is done reading the stage (every compute warp calls it once per stage)
     __device__ void stage_release() {
-        __syncthreads();
-        if (tid == 0 && !*reinterpret_cast<volatile int*>(&sh.abort)) {
-            fence_proxy_async_smem();   // generic writes to the slot before the async refill
-            issue_next();
-        }
+        __syncwarp();
+        if ((tid & 31) == 0) mbar_arrive(&sh.empty_bar[cons % PS_S]);
         ++cons;
+    }
+    __device__ static void csync() { named_sync(PS_CBAR, PS_CT); }
+
+    // producer warp, lane 0: stream every stage of the CTA's step through the
+    // ring; each stage is resolved while its slot is still in use, so a freed
+    // slot is refilled by the copy instructions alone
+    __device__ void produce() {
+        PsCursor c;
+        c.p = 0;
+        c.loc = 0;
+        c.nst = -1;
+        PsStage s;
+        volatile int* ab = &sh.abort;
+        bool have = next(c, s);
+        int i = 0;
+        for (; have && !*ab; ++i) {
+            const int slot = i % PS_S;
+            if (i >= PS_S && !mbar_wait(&sh.empty_bar[slot], ((i / PS_S) - 1) & 1)) {
+                *ab = 1;
+                atomicOr(P.err, FAULT_WAIT);
+                break;
+            }
+            issue(s, slot);
+            have = next(c, s);
+        }
+        // no copy may still be landing when the CTA exits (after an abort some were never consumed)
+        for (int j = max(0, i - PS_S); j < i; ++j)
+            if (!mbar_wait(&sh.full_bar[j % PS_S], (j / PS_S) & 1)) atomicOr(P.err, FAULT_WAIT);
     }
 
     __device__ void grid_arrive(int p) {
-        __syncthreads();
+        csync();
         if (tid == 0) {
             __threadfence();
             atomicAdd(P.bar + p, 1u);
@@ -265,91 +360,125 @@ struct PsState {
             }
             __threadfence();
         }
-        __syncthreads();
+        csync();
     }
 };
 
 // ---------------- GEMV phase ----------------
+// Sum RU values over the warp with RU/2 + RU/4 + ... + 5 - log2(RU) shuffles
+// (each level halves the rows a lane carries); returns the total of row `row`,
+// held by the lanes whose low 5 - log2(RU) bits are zero.
+template <int RU>
+__device__ __forceinline__ float rows_reduce(float (&v)[RU], int lane, int& row) {
+    row = 0;
+    int off = 16;
+#pragma unroll
+    for (int h = RU / 2; h >= 1; h /= 2) {
+        const bool up = (lane & off) != 0;
+#pragma unroll
+        for (int u = 0; u < h; ++u) {
+            const float send = up ? v[u] : v[u + h];
+            const float keep = up ? v[u + h] : v[u];
+            v[u] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+        if (up) row += h;
+        off >>= 1;
+    }
+    float t = v[0];
+#pragma unroll
+    for (int o = 16 / RU; o >= 1; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    return t;
+}
+
+// One GEMV phase over this CTA's rows: warp w owns K-slice w of every row, with
+// the slice's activations in registers; each lane's partial sums are reduced
+// over the warp, the slices' sums wait in shared memory and are added in slice
+// order (fixed order: no atomics) when a chunk of PS_RED_ROWS rows is complete.
+// Stages carry no CTA-wide barrier: a warp releases a stage when it is done.
 template <int CPL, int PRO, int EPI, int HD, int G, bool PAGED>
 __device__ __forceinline__ void ps_gemv(PsState<HD, G, PAGED>& st, const GvGeom& g, const float* act,
                                         int act_stride, const __nv_bfloat16* gain, float* out, int out_stride) {
+    using ST = PsState<HD, G, PAGED>;
     constexpr int VEC = 8;
-    constexpr int RU = 8 / CPL;
+    // rows per pass: a slot holds PS_SLOT / (4096 CPL) rows of K = 2048 CPL (rounded to a power of two)
+    constexpr int RU0 = PS_SLOT / (4096 * CPL) > 0 ? PS_SLOT / (4096 * CPL) : 1;
+    constexpr int RU = RU0 >= 16 ? 16 : (RU0 >= 8 ? 8 : (RU0 >= 4 ? 4 : (RU0 >= 2 ? 2 : 1)));
+    static_assert((RU & (RU - 1)) == 0, "rows per pass must be a power of two");
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int K = g.K;
     const int SWV = K / (PS_SL * VEC);
-    const int slice = warp % PS_SL, grp = warp / PS_SL;
+    const int slice = warp;
     const int vbase = slice * SWV;
     int row0, row1;
     st.rows_of(g.N, row0, row1);
     const int rps = g.rps;
     const int nst = (row1 - row0 + rps - 1) / rps;
+    const int chunk = (PS_RED_ROWS / rps) * rps;   // rows per flush, whole stages
     const size_t row_bytes = (size_t)K * 2;
     PsShared& sh = st.sh;
 
-    // prologue: activations of this lane's columns, in registers
-    float inv = 1.f;
-    if (PRO == PRO_RMSNORM) {
-        float ss = 0.f;
-        for (int k = tid * 4; k < K; k += PS_THREADS * 4) {
-            const float4 x = ldcg4(act + k);
-            ss = fmaf(x.x, x.x, ss);
-            ss = fmaf(x.y, x.y, ss);
-            ss = fmaf(x.z, x.z, ss);
-            ss = fmaf(x.w, x.w, ss);
-        }
-        ss = warp_sum(ss);
-        if (lane == 0) sh.nrm[warp] = ss;
-        __syncthreads();
-        float t = 0.f;
-#pragma unroll
-        for (int w = 0; w < PS_WARPS; ++w) t += sh.nrm[w];
-        inv = 1.0f / sqrtf(t / (float)K + st.P.eps);
-    }
+    // prologue: this lane's activations (its slice columns), in registers; the
+    // slices of the compute warps cover K exactly, so they also give the norm
     float areg[CPL][VEC];
 #pragma unroll
     for (int j = 0; j < CPL; ++j) {
         const int c = (vbase + lane + 32 * j) * VEC;
         const float4 x0 = ldcg4(act + c), x1 = ldcg4(act + c + 4);
-        float o[VEC] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-        if (PRO == PRO_RMSNORM) {
-            float gf[VEC];
-            Elem<__nv_bfloat16>::unpack(*reinterpret_cast<const uint4*>(gain + c), gf);
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) o[e] = o[e] * inv * gf[e];
-        } else if (PRO == PRO_SWIGLU) {
+        areg[j][0] = x0.x; areg[j][1] = x0.y; areg[j][2] = x0.z; areg[j][3] = x0.w;
+        areg[j][4] = x1.x; areg[j][5] = x1.y; areg[j][6] = x1.z; areg[j][7] = x1.w;
+        if (PRO == PRO_SWIGLU) {
             const float4 u0 = ldcg4(act + K + c), u1 = ldcg4(act + K + c + 4);
             const float uu[VEC] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) o[e] = o[e] / (1.0f + expf(-o[e])) * uu[e];
+            for (int e = 0; e < VEC; ++e) areg[j][e] = areg[j][e] / (1.0f + expf(-areg[j][e])) * uu[e];
         }
+    }
+    if (PRO == PRO_RMSNORM) {
+        float ss = 0.f;
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) areg[j][e] = o[e];
+        for (int j = 0; j < CPL; ++j)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) ss = fmaf(areg[j][e], areg[j][e], ss);
+        ss = warp_sum(ss);
+        if (lane == 0) sh.nrm[warp] = ss;
+        ST::csync();
+        float t = 0.f;
+#pragma unroll
+        for (int w = 0; w < PS_CW; ++w) t += sh.nrm[w];
+        const float inv = 1.0f / sqrtf(t / (float)K + st.P.eps);
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) {
+            float gf[VEC];
+            Elem<__nv_bfloat16>::unpack(*reinterpret_cast<const uint4*>(gain + (vbase + lane + 32 * j) * VEC), gf);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) areg[j][e] = areg[j][e] * inv * gf[e];
+        }
     }
     const bool res_local = EPI == EPI_ADD && (row1 - row0) <= PS_MAX_RES;
-    if (EPI == EPI_ADD && res_local)
-        for (int i = tid; i < row1 - row0; i += PS_THREADS) sh.res[i] = __ldcg(out + row0 + i);
-    if (EPI == EPI_ADD) __syncthreads();
+    if (EPI == EPI_ADD && res_local)   // read before this phase writes any row; used after a barrier
+        for (int i = tid; i < row1 - row0; i += PS_CT) sh.res[i] = __ldcg(out + row0 + i);
 
     unsigned long long best = 0ull;
     bool nonfin = false;
+    bool live_all = true;
+    int c0 = 0;   // first row (within the CTA's rows) of the pending chunk
     for (int k = 0; k < nst; ++k) {
-        const int a = row0 + k * rps;
-        const int nr = min(rps, row1 - a);
+        const int a = k * rps;   // first row of the stage, within the CTA's rows
+        const int nr = min(rps, row1 - row0 - a);
         const unsigned char* stg = st.stage_wait();
         const bool live = !*reinterpret_cast<volatile int*>(&sh.abort);
-        const int nmine = nr > grp ? (nr - grp + PS_GR - 1) / PS_GR : 0;
-        for (int m0 = 0; m0 < nmine; m0 += RU) {
+        live_all = live_all && live;
+        for (int m0 = 0; m0 < nr; m0 += RU) {
             float acc[RU], acc2[RU];
 #pragma unroll
             for (int u = 0; u < RU; ++u) acc[u] = acc2[u] = 0.f;
+            // slices are exactly 32 * CPL vectors wide (the plan admits no other K);
+            // rows of the last pass beyond nr re-read row nr - 1, results dropped
             if (live) {
-                // slices are exactly 32 * CPL vectors wide (the plan admits no other K);
-                // a row group's last rows past nmine re-read its last row, results dropped
                 uint4 wv[RU][CPL];
 #pragma unroll
                 for (int u = 0; u < RU; ++u) {
-                    const int iu = grp + PS_GR * min(m0 + u, nmine - 1);
+                    const int iu = min(m0 + u, nr - 1);
                     const uint4* wr = reinterpret_cast<const uint4*>(stg + (size_t)iu * row_bytes);
 #pragma unroll
                     for (int j = 0; j < CPL; ++j) wv[u][j] = wr[vbase + lane + 32 * j];
@@ -368,30 +497,39 @@ __device__ __forceinline__ void ps_gemv(PsState<HD, G, PAGED>& st, const GvGeom&
                     }
             }
 #pragma unroll
-            for (int u = 0; u < RU; ++u) {
-                const float t = warp_sum(acc[u] + acc2[u]);
-                if (lane == 0 && m0 + u < nmine) sh.red[k & 1][grp + PS_GR * (m0 + u)][slice] = t;
-            }
+            for (int u = 0; u < RU; ++u) acc[u] += acc2[u];
+            int ru;
+            const float t = rows_reduce<RU>(acc, lane, ru);
+            if ((lane & (32 / RU - 1)) == 0 && m0 + ru < nr) sh.red[a - c0 + m0 + ru][slice] = t;
         }
         st.stage_release();
-        if (warp == 0 && lane < nr && live) {
-            const int row = a + lane;
-            float t = 0.f;
+        // a full chunk (or the phase's last rows): add the slices, write the rows
+        const int done = a + nr;
+        if (done - c0 == chunk || k == nst - 1) {
+            ST::csync();
+            if (live_all) {
+                for (int i = tid; i < done - c0; i += PS_CT) {
+                    const int row = row0 + c0 + i;
+                    float t = 0.f;
 #pragma unroll
-            for (int w = 0; w < PS_SL; ++w) t += sh.red[k & 1][lane][w];
-            if (EPI == EPI_ADD) {
-                out[row] = (res_local ? sh.res[row - row0] : __ldcg(out + row)) + t;
-            } else {
-                out[row] = t;
+                    for (int w = 0; w < PS_SL; ++w) t += sh.red[i][w];
+                    if (EPI == EPI_ADD) {
+                        out[row] = (res_local ? sh.res[row - row0] : __ldcg(out + row)) + t;
+                    } else {
+                        out[row] = t;
+                    }
+                    if (EPI == EPI_LOGITS) {
+                        if (!isfinite(t)) nonfin = true;
+                        const unsigned long long key = argmax_key(t, row);
+                        best = key > best ? key : best;
+                    }
+                }
             }
-            if (EPI == EPI_LOGITS) {
-                if (!isfinite(t)) nonfin = true;
-                const unsigned long long key = argmax_key(t, row);
-                best = key > best ? key : best;
-            }
+            ST::csync();
+            c0 = done;
         }
     }
-    if (EPI == EPI_LOGITS && warp == 0) {
+    if (EPI == EPI_LOGITS) {
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
@@ -431,12 +569,12 @@ __device__ __forceinline__ void ps_attention(PsState<HD, G, PAGED>& st, int l, f
         const float* qrow = P.qkv + (size_t)r * (P.Hq + 2 * P.Hkv) * HD;
         const float2* rt = P.rope + (size_t)pos * (HD / 2);
         if (PAGED) {   // page ids this unit's producer read
-            for (int q = j0 + tid * Pg; q < j1; q += PS_THREADS * Pg) {
+            for (int q = j0 + tid * Pg; q < j1; q += PS_CT * Pg) {
                 const int pg = P.slot_map[(size_t)r * P.pages_per_row + q / Pg];
                 if (pg < 0 || pg >= P.num_pages) atomicOr(P.err, FAULT_SLOT_MAP);
             }
         }
-        for (int i = tid; i < G * (HD / 2); i += PS_THREADS) {
+        for (int i = tid; i < G * (HD / 2); i += PS_CT) {
             const int h = i / (HD / 2), d = i % (HD / 2);
             const float* qh = qrow + (size_t)(g * G + h) * HD;
             const float a = __ldcg(qh + d), b = __ldcg(qh + d + HD / 2);
@@ -461,28 +599,28 @@ __device__ __forceinline__ void ps_attention(PsState<HD, G, PAGED>& st, int l, f
             } else {
                 off = (((size_t)r * P.Hkv + g) * P.cap + pos) * HD;
             }
-            for (int d = tid; d < HD / 2; d += PS_THREADS) {
+            for (int d = tid; d < HD / 2; d += PS_CT) {
                 const float a = __ldcg(kh + d), b = __ldcg(kh + d + HD / 2);
                 const float2 cs = rt[d];
                 const float k0 = a * cs.x - b * cs.y, k1 = a * cs.y + b * cs.x;
                 kn_s[d] = ok ? Elem<__nv_bfloat16>::round_store(k0, Kc + off + d) : bf16_round_f(k0);
                 kn_s[d + HD / 2] = ok ? Elem<__nv_bfloat16>::round_store(k1, Kc + off + d + HD / 2) : bf16_round_f(k1);
             }
-            for (int d = tid; d < HD; d += PS_THREADS) {
+            for (int d = tid; d < HD; d += PS_CT) {
                 const float vv = __ldcg(vh + d);
                 vn_s[d] = ok ? Elem<__nv_bfloat16>::round_store(vv, Vc + off + d) : bf16_round_f(vv);
             }
         }
-        __syncthreads();
+        ST::csync();
         // Q as the MMA's A operand, a padded bf16 tile [16][HD + 8]: rows g < G hold
         // bf16(q) of head g, rows 8 + g the remainder q - bf16(q), the rest zero
-        for (int i = tid; i < 16 * HD; i += PS_THREADS) {
+        for (int i = tid; i < 16 * HD; i += PS_CT) {
             const int row = i / HD, col = i % HD, h = row & 7;
             const float v = h < G ? q_s[h * HD + col] : 0.f;
             const float hi = bf16_round_f(v);
             qt_s[row * (HD + 8) + col] = __float2bfloat16_rn(row < 8 ? hi : v - hi);
         }
-        __syncthreads();
+        ST::csync();
 
         // O^T accumulators: tile dt covers dims 16dt..16dt+15 (rows g, g + 8) x
         // columns 2tq, 2tq+1 (columns 0..3: heads' bf16 parts, 4..7: remainders)
@@ -501,7 +639,7 @@ __device__ __forceinline__ void ps_attention(PsState<HD, G, PAGED>& st, int l, f
             const int p0 = j0 + t * PPS;
             if (owner && pos >= p0 && pos < p0 + PPS) {   // CTA-uniform
                 const int row = pos - p0;
-                for (int i = tid; i < 2 * (HD / 8); i += PS_THREADS) {
+                for (int i = tid; i < 2 * (HD / 8); i += PS_CT) {
                     const int c = i % (HD / 8);
                     const float* src = (i < HD / 8 ? kn_s : vn_s) + c * 8;
                     uint4 v;
@@ -511,7 +649,8 @@ __device__ __forceinline__ void ps_attention(PsState<HD, G, PAGED>& st, int l, f
                     v.w = pack_bf16x2(src[6], src[7]);
                     *reinterpret_cast<uint4*>((i < HD / 8 ? kt : vt) + swz<HD, PPS>(row, c)) = v;
                 }
-                __syncthreads();
+                fence_proxy_async_smem();   // these generic writes before the slot's next async refill
+                ST::csync();
             }
             if (live && warp < PS_AW) {
 #pragma unroll
@@ -637,8 +776,8 @@ __device__ __forceinline__ void ps_attention(PsState<HD, G, PAGED>& st, int l, f
                 sh.wl[warp][gq] = lsum;
             }
         }
-        __syncthreads();
-        for (int i = tid; i < G * HD; i += PS_THREADS) {
+        ST::csync();
+        for (int i = tid; i < G * HD; i += PS_CT) {
             const int h = i / HD, d = i % HD;
             float M = -INFINITY;
 #pragma unroll
@@ -658,24 +797,24 @@ __device__ __forceinline__ void ps_attention(PsState<HD, G, PAGED>& st, int l, f
             }
         }
         __threadfence();
-        __syncthreads();
+        ST::csync();
         if (tid == 0) {
             const unsigned prev = atomicAdd(P.counters + r * P.Hkv + g, 1u);
             sh.last = prev == (unsigned)P.nsplit - 1u;
         }
-        __syncthreads();
+        ST::csync();
         if (sh.last) {
             __threadfence();
             if (tid == 0) P.counters[r * P.Hkv + g] = 0u;
             const int NS = P.nsplit;
-            for (int i = tid; i < G * NS; i += PS_THREADS) {
+            for (int i = tid; i < G * NS; i += PS_CT) {
                 const int h = i / NS, ss = i % NS;
                 const float* pp = P.part + (((size_t)r * P.Hq + g * G + h) * NS + ss) * (HD + 4);
                 sh.cm[h * NS + ss] = __ldcg(pp);
                 sh.cw[h * NS + ss] = __ldcg(pp + 1);
             }
-            __syncthreads();
-            for (int h = warp; h < G; h += PS_WARPS) {
+            ST::csync();
+            for (int h = warp; h < G; h += PS_CW) {
                 float M = -INFINITY;
                 for (int ss = lane; ss < NS; ss += 32) M = fmaxf(M, sh.cm[h * NS + ss]);
                 M = warp_max(M);
@@ -690,8 +829,8 @@ __device__ __forceinline__ void ps_attention(PsState<HD, G, PAGED>& st, int l, f
                     sh.cw[h * NS + ss] = (mm == -INFINITY) ? 0.f : expf(mm - M) / Lsum;
                 }
             }
-            __syncthreads();
-            for (int i = tid; i < G * HD; i += PS_THREADS) {
+            ST::csync();
+            for (int i = tid; i < G * HD; i += PS_CT) {
                 const int h = i / HD, d = i % HD;
                 const float* base = P.part + (((size_t)r * P.Hq + g * G + h) * NS) * (HD + 4) + 4 + d;
                 float acc = 0.f;
@@ -700,7 +839,7 @@ __device__ __forceinline__ void ps_attention(PsState<HD, G, PAGED>& st, int l, f
                 P.attn[(size_t)r * P.Hq * HD + (size_t)(g * G + h) * HD + d] = acc;
             }
         }
-        __syncthreads();
+        ST::csync();
     }
 }
 
@@ -718,85 +857,91 @@ __global__ void __launch_bounds__(PS_THREADS, 1) k_persist(const __grid_constant
 
     for (int i = tid; i < P.L * 9; i += PS_THREADS) sh.wtab[i] = P.lw[i];
     if (tid == 0) {
-        for (int s = 0; s < PS_S; ++s) mbar_init(&sh.full_bar[s], 1);
+        for (int s = 0; s < PS_S; ++s) {
+            mbar_init(&sh.full_bar[s], 1);
+            mbar_init(&sh.empty_bar[s], PS_CW);
+        }
         sh.abort = 0;
         mbar_fence_init();
     }
     __syncthreads();
     ST st(P, sh, ring);
-    if (tid == 0)
-        for (int i = 0; i < PS_S; ++i) st.issue_next();   // the stream starts before any dependency
     const int np = st.np;
 
-    for (int p = 0; p < np; ++p) {
-        const int k = st.kind(p);
-        if (tid == 0) trace_stamp(P.trace, p, 0);
-        if (p > 0) st.grid_wait(p - 1);
-        if (tid == 0) trace_stamp(P.trace, p, 1);
-        if (k == PK_EMBED) {
-            if (st.cta == 0) {
-                // the step's first phase: resets, checks, gather (as k_embed)
-                if (tid == 0) *P.err = 0u;
-                if (tid < P.R) {
-                    P.amax[tid] = 0ull;
-                    P.nonfinite[tid] = 0u;
+    if (tid >= PS_CT) {
+        // producer warp: the CTA's whole weight / KV stream, independent of the
+        // phases' grid-wide dependencies (it only waits for free ring slots)
+        if (tid == PS_CT) st.produce();
+        __syncwarp();
+    } else {
+        for (int p = 0; p < np; ++p) {
+            const int k = st.kind(p);
+            if (tid == 0) trace_stamp(P.trace, p, 0);
+            if (p > 0) st.grid_wait(p - 1);
+            if (tid == 0) trace_stamp(P.trace, p, 1);
+            if (k == PK_EMBED) {
+                if (st.cta == 0) {
+                    // the step's first phase: resets, checks, gather (as k_embed)
+                    if (tid == 0) *P.err = 0u;
+                    if (tid < P.R) {
+                        P.amax[tid] = 0ull;
+                        P.nonfinite[tid] = 0u;
+                    }
+                    ST::csync();
+                    for (int r = 0; r < P.R; ++r) {
+                        int tok = P.slots[r];
+                        const int pos = P.slots[P.R + r];
+                        if (tok < 0 || tok >= P.V) {
+                            if (tid == 0) atomicOr(P.err, FAULT_TOKEN);
+                            tok = 0;
+                        }
+                        if ((pos < 0 || pos >= P.cap) && tid == 0) atomicOr(P.err, FAULT_POS);
+                        const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(P.embed) + (size_t)tok * P.d;
+                        for (int i = tid * 8; i < P.d; i += PS_CT * 8) {
+                            float f[8];
+                            Elem<__nv_bfloat16>::unpack(*reinterpret_cast<const uint4*>(e + i), f);
+                            *reinterpret_cast<float4*>(P.x + i + (size_t)r * P.d) = make_float4(f[0], f[1], f[2], f[3]);
+                            *reinterpret_cast<float4*>(P.x + i + 4 + (size_t)r * P.d) =
+                                make_float4(f[4], f[5], f[6], f[7]);
+                        }
+                    }
                 }
-                __syncthreads();
-                for (int r = 0; r < P.R; ++r) {
-                    int tok = P.slots[r];
-                    const int pos = P.slots[P.R + r];
-                    if (tok < 0 || tok >= P.V) {
-                        if (tid == 0) atomicOr(P.err, FAULT_TOKEN);
-                        tok = 0;
-                    }
-                    if ((pos < 0 || pos >= P.cap) && tid == 0) atomicOr(P.err, FAULT_POS);
-                    const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(P.embed) + (size_t)tok * P.d;
-                    for (int i = tid * 8; i < P.d; i += PS_THREADS * 8) {
-                        float f[8];
-                        Elem<__nv_bfloat16>::unpack(*reinterpret_cast<const uint4*>(e + i), f);
-                        *reinterpret_cast<float4*>(P.x + i + (size_t)r * P.d) = make_float4(f[0], f[1], f[2], f[3]);
-                        *reinterpret_cast<float4*>(P.x + i + 4 + (size_t)r * P.d) = make_float4(f[4], f[5], f[6], f[7]);
-                    }
+            } else if (k == PK_ATTN) {
+                ps_attention<HD, G, PAGED>(st, st.layer(p), q_s, kn_s, vn_s, wo_s, qt_s);
+            } else {
+                GvGeom g;
+                const int l = k == PK_HEAD ? 0 : st.layer(p);
+                st.geom(k, l, g);
+                const __nv_bfloat16* w9 = nullptr;
+                switch (k) {
+                    case PK_QKV:
+                        ps_gemv<CPL_D, PRO_RMSNORM, EPI_STORE>(st, g, P.x, P.d,
+                            reinterpret_cast<const __nv_bfloat16*>(sh.wtab[l * 9 + 0]), P.qkv, g.N);
+                        break;
+                    case PK_O:
+                        ps_gemv<CPL_D, PRO_PLAIN, EPI_ADD>(st, g, P.attn, g.K, w9, P.x, P.d);
+                        break;
+                    case PK_GU:
+                        ps_gemv<CPL_D, PRO_RMSNORM, EPI_STORE>(st, g, P.x, P.d,
+                            reinterpret_cast<const __nv_bfloat16*>(sh.wtab[l * 9 + 5]), P.gu, g.N);
+                        break;
+                    case PK_DOWN:
+                        ps_gemv<CPL_F, PRO_SWIGLU, EPI_ADD>(st, g, P.gu, 2 * P.F, w9, P.x, P.d);
+                        break;
+                    default:
+                        ps_gemv<CPL_D, PRO_RMSNORM, EPI_LOGITS>(st, g, P.x, P.d,
+                            reinterpret_cast<const __nv_bfloat16*>(P.final_norm), P.logits, P.V);
+                        break;
                 }
             }
-        } else if (k == PK_ATTN) {
-            ps_attention<HD, G, PAGED>(st, st.layer(p), q_s, kn_s, vn_s, wo_s, qt_s);
-        } else {
-            GvGeom g;
-            const int l = k == PK_HEAD ? 0 : st.layer(p);
-            st.geom(k, l, g);
-            const __nv_bfloat16* w9 = nullptr;
-            switch (k) {
-                case PK_QKV:
-                    ps_gemv<CPL_D, PRO_RMSNORM, EPI_STORE>(st, g, P.x, P.d,
-                        reinterpret_cast<const __nv_bfloat16*>(sh.wtab[l * 9 + 0]), P.qkv, g.N);
-                    break;
-                case PK_O:
-                    ps_gemv<CPL_D, PRO_PLAIN, EPI_ADD>(st, g, P.attn, g.K, w9, P.x, P.d);
-                    break;
-                case PK_GU:
-                    ps_gemv<CPL_D, PRO_RMSNORM, EPI_STORE>(st, g, P.x, P.d,
-                        reinterpret_cast<const __nv_bfloat16*>(sh.wtab[l * 9 + 5]), P.gu, g.N);
-                    break;
-                case PK_DOWN:
-                    ps_gemv<CPL_F, PRO_SWIGLU, EPI_ADD>(st, g, P.gu, 2 * P.F, w9, P.x, P.d);
-                    break;
-                default:
-                    ps_gemv<CPL_D, PRO_RMSNORM, EPI_LOGITS>(st, g, P.x, P.d,
-                        reinterpret_cast<const __nv_bfloat16*>(P.final_norm), P.logits, P.V);
-                    break;
+            st.grid_arrive(p);
+            if (tid == 0) {
+                trace_stamp(P.trace, p, 2);
+                trace_stamp(P.trace, p, 3);
             }
-        }
-        st.grid_arrive(p);
-        if (tid == 0) {
-            trace_stamp(P.trace, p, 2);
-            trace_stamp(P.trace, p, 3);
         }
     }
-    // no copy may still be landing when the CTA exits
-    if (tid == 0)
-        for (int i = max(0, st.iss_tot - PS_S); i < st.iss_tot; ++i)
-            if (!mbar_wait(&sh.full_bar[i % PS_S], (i / PS_S) & 1)) atomicOr(P.err, FAULT_WAIT);
+    __syncthreads();   // the producer has seen its last copy land
     // the last CTA out resets the grid counters for the next replay
     if (tid == 0) {
         __threadfence();
@@ -838,13 +983,14 @@ cudaError_t persist_plan(PersistPlan* plan, int num_sms) {
     auto rps_for = [&](int K, int cpl) {
         int r = PS_SLOT / (K * 2);
         if (r > PS_MAX_RPS) r = PS_MAX_RPS;
-        const int ru = 8 / cpl;
-        if (r >= PS_GR * ru) r -= r % (PS_GR * ru);
+        int ru0 = PS_SLOT / (4096 * cpl), ru = 1;   // the kernel's rows per pass
+        while (ru * 2 <= ru0 && ru < 16) ru *= 2;
+        if (r >= ru) r -= r % ru;
         return r;
     };
     p.rps_d = rps_for(p.d, cd);
     p.rps_f = rps_for(p.F, cf);
-    if (p.rps_d < PS_GR || p.rps_f < PS_GR) return cudaErrorNotSupported;
+    if (p.rps_d < 1 || p.rps_f < 1) return cudaErrorNotSupported;
     // attention splits: whole half-stages; units spread over the grid
     const int pps = PS_SLOT / (2 * p.hd * 2), half = pps / 2;
     if (p.paged ? (pps % p.page != 0 || p.cap % p.page != 0) : (p.cap % half != 0)) return cudaErrorNotSupported;
