@@ -158,6 +158,7 @@ struct PersistParams {
     unsigned long long* trace;
     int split_len, nsplit;
     int rps_d, rps_f;          // weight rows per ring stage for K = d and K = F
+    int pf;                    // stages beyond the ring's reach prefetched into L2 by the producer
 };
 
 struct PersistPlan {

@@ -56,6 +56,8 @@ constexpr int PS_MAX_NS = 64;              // attention splits per (row, kv head
 constexpr uint32_t PS_SPIN = 1u << 24;     // polls of a grid-wide wait
 
 enum { PK_EMBED = 0, PK_QKV = 1, PK_ATTN = 2, PK_O = 3, PK_GU = 4, PK_DOWN = 5, PK_HEAD = 6 };
+// gate/up phase: a CTA owns gate rows [a, b) and up rows [a, b) and writes silu(gate) * up
+constexpr int EPI_SWIGLU_PAIR = 3;
 
 __device__ __forceinline__ float4 ldcg4(const float* p) { return __ldcg(reinterpret_cast<const float4*>(p)); }
 __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
@@ -170,9 +172,26 @@ struct PsState {
         } else {
             GvGeom g;
             geom(c.kind, c.layer, g);
+            const uint32_t rb = (uint32_t)g.K * 2u;
+            if (c.kind == PK_GU) {   // gate rows [a, b), then up rows [a, b)
+                int a, b;
+                rows_of(g.n[0], a, b);
+                c.rs0 = static_cast<const unsigned char*>(g.w[0]) + (size_t)a * rb;
+                c.rs1 = static_cast<const unsigned char*>(g.w[1]) + (size_t)a * rb;
+                c.rs2 = c.rs1;
+                c.rb0 = c.rb1 = (uint32_t)(b - a) * rb;
+                c.rb2 = 0u;
+                c.nruns = b > a ? 2 : 0;
+                c.run = 0;
+                c.src = c.rs0;
+                c.run_left = c.nruns ? c.rb0 : 0u;
+                c.stage_bytes = (uint32_t)g.rps * rb;
+                c.phase_left = 2u * (uint32_t)(b - a) * rb;
+                c.nst = (2 * (b - a) + g.rps - 1) / g.rps;
+                return;
+            }
             int r0, r1;
             rows_of(g.N, r0, r1);
-            const uint32_t rb = (uint32_t)g.K * 2u;
             // the CTA's rows [r0, r1) cut by the segments [0, n0), [n0, n0 + n1), [n0 + n1, N)
             const int e0 = g.n[0], e1 = g.n[0] + g.n[1];
             const int a0 = r0, z0 = min(r1, e0);
@@ -307,6 +326,36 @@ struct PsState {
     }
     __device__ static void csync() { named_sync(PS_CBAR, PS_CT); }
 
+    // the bytes of stage s into L2 (a hint; no shared memory involved)
+    __device__ void prefetch(const PsStage& s) const {
+        if (s.kind != PK_ATTN) {
+            if (s.b0) prefetch_l2_bulk(s.s0, s.b0);
+            if (s.b1) prefetch_l2_bulk(s.s1, s.b1);
+            if (s.b2) prefetch_l2_bulk(s.s2, s.b2);
+            return;
+        }
+        const int l = s.layer, u = s.u;
+        const int sp = u % P.nsplit, g = (u / P.nsplit) % P.Hkv, r = u / (P.nsplit * P.Hkv);
+        const int j0 = sp * P.split_len;
+        const int j1 = min(j0 + P.split_len, P.cap);
+        const int p0 = j0 + s.uloc * PPS, p1 = min(p0 + PPS, j1);
+        const unsigned char* kb = static_cast<const unsigned char*>(P.kv[2 * l]);
+        const unsigned char* vb = static_cast<const unsigned char*>(P.kv[2 * l + 1]);
+        if (PAGED) {
+            for (int q = p0; q < p1; q += P.page) {
+                int pg = P.slot_map[(size_t)r * P.pages_per_row + q / P.page];
+                if (pg < 0 || pg >= P.num_pages) pg = 0;
+                const size_t off = (size_t)((pg * P.Hkv + g) * P.page) * HD * 2;
+                prefetch_l2_bulk(kb + off, (unsigned)(P.page * HD * 2));
+                prefetch_l2_bulk(vb + off, (unsigned)(P.page * HD * 2));
+            }
+        } else {
+            const size_t off = (size_t)((r * P.Hkv + g) * P.cap + p0) * HD * 2;
+            prefetch_l2_bulk(kb + off, (unsigned)((p1 - p0) * HD * 2));
+            prefetch_l2_bulk(vb + off, (unsigned)((p1 - p0) * HD * 2));
+        }
+    }
+
     // producer warp, lane 0: stream every stage of the CTA's step through the
     // ring; each stage is resolved while its slot is still in use, so a freed
     // slot is refilled by the copy instructions alone
@@ -318,6 +367,10 @@ struct PsState {
         PsStage s;
         volatile int* ab = &sh.abort;
         bool have = next(c, s);
+        // second cursor: L2 prefetches of the next P.pf stages, issued before their slots free
+        PsCursor f = c;
+        PsStage sf;
+        int fi = 1;   // next stage index of f
         int i = 0;
         for (; have && !*ab; ++i) {
             const int slot = i % PS_S;
@@ -328,6 +381,10 @@ struct PsState {
             }
             issue(s, slot);
             have = next(c, s);
+            while (fi <= i + P.pf && next(f, sf)) {   // stages i + 1 .. i + pf, ahead of their slots
+                prefetch(sf);
+                ++fi;
+            }
         }
         // no copy may still be landing when the CTA exits (after an abort some were never consumed)
         for (int j = max(0, i - PS_S); j < i; ++j)
@@ -397,7 +454,7 @@ __device__ __forceinline__ float rows_reduce(float (&v)[RU], int lane, int& row)
 // Stages carry no CTA-wide barrier: a warp releases a stage when it is done.
 template <int CPL, int PRO, int EPI, int HD, int G, bool PAGED>
 __device__ __forceinline__ void ps_gemv(PsState<HD, G, PAGED>& st, const GvGeom& g, const float* act,
-                                        int act_stride, const __nv_bfloat16* gain, float* out, int out_stride) {
+                                        const __nv_bfloat16* gain, float* out, int phase) {
     using ST = PsState<HD, G, PAGED>;
     constexpr int VEC = 8;
     // rows per pass: a slot holds PS_SLOT / (4096 CPL) rows of K = 2048 CPL (rounded to a power of two)
@@ -409,13 +466,27 @@ __device__ __forceinline__ void ps_gemv(PsState<HD, G, PAGED>& st, const GvGeom&
     const int SWV = K / (PS_SL * VEC);
     const int slice = warp;
     const int vbase = slice * SWV;
-    int row0, row1;
-    st.rows_of(g.N, row0, row1);
+    int row0, row1;   // the CTA's rows; for the gate/up pair, 2 (b - a) logical rows from row0 = a
+    if (EPI == EPI_SWIGLU_PAIR) {
+        st.rows_of(g.n[0], row0, row1);
+        row1 = row0 + 2 * (row1 - row0);
+    } else {
+        st.rows_of(g.N, row0, row1);
+    }
     const int rps = g.rps;
     const int nst = (row1 - row0 + rps - 1) / rps;
     const int chunk = (PS_RED_ROWS / rps) * rps;   // rows per flush, whole stages
     const size_t row_bytes = (size_t)K * 2;
     PsShared& sh = st.sh;
+
+    // the norm gains do not depend on the previous phase: load them before its wait
+    uint4 graw[PRO == PRO_RMSNORM ? CPL : 1];
+    if (PRO == PRO_RMSNORM) {
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) graw[j] = *reinterpret_cast<const uint4*>(gain + (vbase + lane + 32 * j) * VEC);
+    }
+    st.grid_wait(phase - 1);
+    if (tid == 0) trace_stamp(st.P.trace, phase, 1);
 
     // prologue: this lane's activations (its slice columns), in registers; the
     // slices of the compute warps cover K exactly, so they also give the norm
@@ -426,12 +497,6 @@ __device__ __forceinline__ void ps_gemv(PsState<HD, G, PAGED>& st, const GvGeom&
         const float4 x0 = ldcg4(act + c), x1 = ldcg4(act + c + 4);
         areg[j][0] = x0.x; areg[j][1] = x0.y; areg[j][2] = x0.z; areg[j][3] = x0.w;
         areg[j][4] = x1.x; areg[j][5] = x1.y; areg[j][6] = x1.z; areg[j][7] = x1.w;
-        if (PRO == PRO_SWIGLU) {
-            const float4 u0 = ldcg4(act + K + c), u1 = ldcg4(act + K + c + 4);
-            const float uu[VEC] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) areg[j][e] = areg[j][e] / (1.0f + expf(-areg[j][e])) * uu[e];
-        }
     }
     if (PRO == PRO_RMSNORM) {
         float ss = 0.f;
@@ -449,7 +514,7 @@ __device__ __forceinline__ void ps_gemv(PsState<HD, G, PAGED>& st, const GvGeom&
 #pragma unroll
         for (int j = 0; j < CPL; ++j) {
             float gf[VEC];
-            Elem<__nv_bfloat16>::unpack(*reinterpret_cast<const uint4*>(gain + (vbase + lane + 32 * j) * VEC), gf);
+            Elem<__nv_bfloat16>::unpack(graw[j], gf);
 #pragma unroll
             for (int e = 0; e < VEC; ++e) areg[j][e] = areg[j][e] * inv * gf[e];
         }
@@ -507,7 +572,18 @@ __device__ __forceinline__ void ps_gemv(PsState<HD, G, PAGED>& st, const GvGeom&
         const int done = a + nr;
         if (done - c0 == chunk || k == nst - 1) {
             ST::csync();
-            if (live_all) {
+            if (EPI == EPI_SWIGLU_PAIR && live_all) {   // one flush holds both halves (the plan checks it)
+                const int n = (row1 - row0) / 2;
+                for (int i = tid; i < n; i += PS_CT) {
+                    float gs = 0.f, us = 0.f;
+#pragma unroll
+                    for (int w = 0; w < PS_SL; ++w) {
+                        gs += sh.red[i][w];
+                        us += sh.red[n + i][w];
+                    }
+                    out[row0 + i] = gs / (1.0f + expf(-gs)) * us;
+                }
+            } else if (live_all) {
                 for (int i = tid; i < done - c0; i += PS_CT) {
                     const int row = row0 + c0 + i;
                     float t = 0.f;
@@ -830,13 +906,39 @@ __device__ __forceinline__ void ps_attention(PsState<HD, G, PAGED>& st, int l, f
                 }
             }
             ST::csync();
-            for (int i = tid; i < G * HD; i += PS_CT) {
-                const int h = i / HD, d = i % HD;
-                const float* base = P.part + (((size_t)r * P.Hq + g * G + h) * NS) * (HD + 4) + 4 + d;
-                float acc = 0.f;
-#pragma unroll 4
-                for (int ss = 0; ss < NS; ++ss) acc = fmaf(sh.cw[h * NS + ss], __ldcg(base + (size_t)ss * (HD + 4)), acc);
-                P.attn[(size_t)r * P.Hq * HD + (size_t)(g * G + h) * HD + d] = acc;
+            // every partial this thread needs is requested before any is used
+            constexpr int PER = (G * HD + PS_CT - 1) / PS_CT;   // outputs per thread
+            constexpr int CH = 16;                              // splits per batch of loads
+            float acc[PER];
+#pragma unroll
+            for (int q = 0; q < PER; ++q) acc[q] = 0.f;
+            for (int s0 = 0; s0 < NS; s0 += CH) {
+                float v[PER][CH];
+#pragma unroll
+                for (int q = 0; q < PER; ++q) {
+                    const int i = tid + q * PS_CT;
+                    const int h = min(i, G * HD - 1) / HD, d = min(i, G * HD - 1) % HD;
+                    const float* base = P.part + (((size_t)r * P.Hq + g * G + h) * NS) * (HD + 4) + 4 + d;
+#pragma unroll
+                    for (int j = 0; j < CH; ++j)
+                        v[q][j] = s0 + j < NS ? __ldcg(base + (size_t)(s0 + j) * (HD + 4)) : 0.f;
+                }
+#pragma unroll
+                for (int q = 0; q < PER; ++q) {
+                    const int h = min(tid + q * PS_CT, G * HD - 1) / HD;
+#pragma unroll
+                    for (int j = 0; j < CH; ++j)
+                        if (s0 + j < NS) acc[q] = fmaf(sh.cw[h * NS + s0 + j], v[q][j], acc[q]);
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < PER; ++q) {
+                const int i = tid + q * PS_CT;
+                if (i < G * HD) {
+                    const int h = i / HD, d = i % HD;
+                    const float out = acc[q];
+                    P.attn[(size_t)r * P.Hq * HD + (size_t)(g * G + h) * HD + d] = out;
+                }
             }
         }
         ST::csync();
@@ -877,8 +979,11 @@ __global__ void __launch_bounds__(PS_THREADS, 1) k_persist(const __grid_constant
         for (int p = 0; p < np; ++p) {
             const int k = st.kind(p);
             if (tid == 0) trace_stamp(P.trace, p, 0);
-            if (p > 0) st.grid_wait(p - 1);
-            if (tid == 0) trace_stamp(P.trace, p, 1);
+            const bool gemv = k != PK_EMBED && k != PK_ATTN;   // GEMV phases wait inside (after their gain loads)
+            if (!gemv) {
+                if (p > 0) st.grid_wait(p - 1);
+                if (tid == 0) trace_stamp(P.trace, p, 1);
+            }
             if (k == PK_EMBED) {
                 if (st.cta == 0) {
                     // the step's first phase: resets, checks, gather (as k_embed)
@@ -915,22 +1020,22 @@ __global__ void __launch_bounds__(PS_THREADS, 1) k_persist(const __grid_constant
                 const __nv_bfloat16* w9 = nullptr;
                 switch (k) {
                     case PK_QKV:
-                        ps_gemv<CPL_D, PRO_RMSNORM, EPI_STORE>(st, g, P.x, P.d,
-                            reinterpret_cast<const __nv_bfloat16*>(sh.wtab[l * 9 + 0]), P.qkv, g.N);
+                        ps_gemv<CPL_D, PRO_RMSNORM, EPI_STORE>(st, g, P.x,
+                            reinterpret_cast<const __nv_bfloat16*>(sh.wtab[l * 9 + 0]), P.qkv, p);
                         break;
                     case PK_O:
-                        ps_gemv<CPL_D, PRO_PLAIN, EPI_ADD>(st, g, P.attn, g.K, w9, P.x, P.d);
+                        ps_gemv<CPL_D, PRO_PLAIN, EPI_ADD>(st, g, P.attn, w9, P.x, p);
                         break;
                     case PK_GU:
-                        ps_gemv<CPL_D, PRO_RMSNORM, EPI_STORE>(st, g, P.x, P.d,
-                            reinterpret_cast<const __nv_bfloat16*>(sh.wtab[l * 9 + 5]), P.gu, g.N);
+                        ps_gemv<CPL_D, PRO_RMSNORM, EPI_SWIGLU_PAIR>(st, g, P.x,
+                            reinterpret_cast<const __nv_bfloat16*>(sh.wtab[l * 9 + 5]), P.gu, p);
                         break;
                     case PK_DOWN:
-                        ps_gemv<CPL_F, PRO_SWIGLU, EPI_ADD>(st, g, P.gu, 2 * P.F, w9, P.x, P.d);
+                        ps_gemv<CPL_F, PRO_PLAIN, EPI_ADD>(st, g, P.gu, w9, P.x, p);
                         break;
                     default:
-                        ps_gemv<CPL_D, PRO_RMSNORM, EPI_LOGITS>(st, g, P.x, P.d,
-                            reinterpret_cast<const __nv_bfloat16*>(P.final_norm), P.logits, P.V);
+                        ps_gemv<CPL_D, PRO_RMSNORM, EPI_LOGITS>(st, g, P.x,
+                            reinterpret_cast<const __nv_bfloat16*>(P.final_norm), P.logits, p);
                         break;
                 }
             }
@@ -991,6 +1096,8 @@ cudaError_t persist_plan(PersistPlan* plan, int num_sms) {
     p.rps_d = rps_for(p.d, cd);
     p.rps_f = rps_for(p.F, cf);
     if (p.rps_d < 1 || p.rps_f < 1) return cudaErrorNotSupported;
+    // gate/up: a CTA's gate and up rows are added in one flush
+    if (2 * ((p.F + num_sms - 1) / num_sms) > (PS_RED_ROWS / p.rps_d) * p.rps_d) return cudaErrorNotSupported;
     // attention splits: whole half-stages; units spread over the grid
     const int pps = PS_SLOT / (2 * p.hd * 2), half = pps / 2;
     if (p.paged ? (pps % p.page != 0 || p.cap % p.page != 0) : (p.cap % half != 0)) return cudaErrorNotSupported;
@@ -1013,6 +1120,7 @@ cudaError_t persist_plan(PersistPlan* plan, int num_sms) {
     }
     p.split_len = bl;
     p.nsplit = bn;
+    p.pf = 0;
     plan->grid = num_sms;
     plan->block = PS_THREADS;
     plan->smem = (size_t)PS_S * PS_SLOT + 1024;
