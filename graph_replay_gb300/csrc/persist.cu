@@ -50,16 +50,50 @@ constexpr int PS_S = 196608 / PS_SLOT;      // ring slots (192 KB of shared memo
 constexpr int PS_MAX_RPS = 32;
 constexpr int PS_MAX_RES = 64;
 constexpr int PS_RED_ROWS = 192;          // rows whose slice partials wait in shared memory
-constexpr int PS_AW = 4;                   // warps that compute attention
-constexpr int PS_MAX_L = 64;               // layers whose weight pointers fit the smem table
+constexpr int PS_AW = PS_CW;               // warps that compute attention
 constexpr int PS_MAX_NS = 64;              // attention splits per (row, kv head)
-constexpr uint32_t PS_SPIN = 1u << 24;     // polls of a grid-wide wait
+constexpr uint32_t PS_SPIN = 1u << 22;     // polls of a grid-wide wait (each an L2 round trip)
 
 enum { PK_EMBED = 0, PK_QKV = 1, PK_ATTN = 2, PK_O = 3, PK_GU = 4, PK_DOWN = 5, PK_HEAD = 6 };
 // gate/up phase: a CTA owns gate rows [a, b) and up rows [a, b) and writes silu(gate) * up
 constexpr int EPI_SWIGLU_PAIR = 3;
 
+// Bounded wait on a ring barrier.  PS_WAIT_MODE 0: try_wait (may suspend for a
+// hardware-chosen time); 1: try_wait with a short suspend-time hint; 2: test_wait spin.
+#ifndef PS_WAIT_MODE
+#define PS_WAIT_MODE 0
+#endif
+__device__ __forceinline__ bool ps_wait(uint64_t* bar, uint32_t parity) {
+#if PS_WAIT_MODE == 0
+    return mbar_wait(bar, parity);
+#else
+    for (uint32_t i = 0; i < MBAR_POLLS * 4u; ++i) {
+        uint32_t ok;
+#if PS_WAIT_MODE == 1
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(parity), "r"(64u)
+            : "memory");
+#else
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(parity)
+            : "memory");
+#endif
+        if (ok) return true;
+    }
+    return false;
+#endif
+}
+
 __device__ __forceinline__ float4 ldcg4(const float* p) { return __ldcg(reinterpret_cast<const float4*>(p)); }
+// release add: this thread's prior writes, and those it has observed through a
+// CTA barrier, are visible at gpu scope before the count is
+__device__ __forceinline__ void red_release(unsigned* p, unsigned v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
     unsigned v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -90,17 +124,38 @@ struct PsStage {
     uint32_t b0, b1, b2;
 };
 
+// shared memory besides the ring; the GEMV and attention phases never overlap,
+// so their scratch shares one union
+// poll until *p >= target (acquire), giving up after PS_SPIN polls or when the
+// grid-wide abort word is set; false if it gave up
+__device__ __forceinline__ bool ps_poll_ge(const unsigned* p, unsigned target, const volatile unsigned* abort_word) {
+    for (uint32_t i = 0; i < PS_SPIN; ++i) {
+        if (ld_acquire(p) >= target) return true;
+        if ((i & 63u) == 63u && *abort_word) return false;
+    }
+    return false;
+}
+
+template <int HD, int G>
 struct PsShared {
     uint64_t full_bar[PS_S];   // a ring slot's copy landed (producer's expect_tx + the copy bytes)
     uint64_t empty_bar[PS_S];  // every compute warp is done with the slot
     int abort;
-    int last;
-    const void* wtab[PS_MAX_L * 9];
-    float red[PS_RED_ROWS][PS_SL];
     float nrm[PS_CW];
-    float res[PS_MAX_RES];
-    float wm[PS_AW][8], wl[PS_AW][8];
-    float cm[8 * PS_MAX_NS], cw[8 * PS_MAX_NS];
+    float wm[PS_AW][8], wl[PS_AW][8], wf[PS_AW][8];   // per (attention warp, head): max, sum, merge factor
+    float hm[8], hl[8];                               // per head: the split's max and sum
+    union {
+        struct {
+            float red[PS_RED_ROWS][PS_SL];   // slice partial sums of pending rows
+            float res[PS_MAX_RES];           // residual rows (EPI_ADD)
+        } gv;
+        struct {
+            float q[G * HD];                 // rotated, scaled query heads of the group
+            float kn[HD], vn[HD];            // the new K / V row (owner of pos)
+            float wo[PS_AW * G * HD];        // per-warp outputs to merge
+            __align__(16) __nv_bfloat16 qt[16 * (HD + 8)];   // Q as the MMA's A tile
+        } at;
+    } sc;
 };
 
 // geometry of a GEMV phase: up to three stacked weight segments
@@ -113,7 +168,7 @@ struct GvGeom {
 template <int HD, int G, bool PAGED>
 struct PsState {
     const PersistParams& P;
-    PsShared& sh;
+    PsShared<HD, G>& sh;
     unsigned char* ring;
     int cta, nc, np, tid;
     int cons;   // stages consumed (uniform over the CTA)
@@ -122,7 +177,7 @@ struct PsState {
     static constexpr int TILE = PPS * HD * 2;            // bytes of the K (or V) tile
     static constexpr int SUB = HD / 64;
 
-    __device__ PsState(const PersistParams& p, PsShared& s, unsigned char* r)
+    __device__ PsState(const PersistParams& p, PsShared<HD, G>& s, unsigned char* r)
         : P(p), sh(s), ring(r), cta(blockIdx.x), nc(gridDim.x), np(5 * p.L + 2), tid(threadIdx.x), cons(0) {}
 
     __device__ int kind(int p) const { return p == 0 ? PK_EMBED : (p == np - 1 ? PK_HEAD : 1 + (p - 1) % 5); }
@@ -132,7 +187,7 @@ struct PsState {
         r1 = (int)(((long long)(cta + 1) * N) / nc);
     }
     __device__ void geom(int k, int l, GvGeom& g) const {
-        const void* const* w = sh.wtab + l * 9;   // attn_norm, q, k, v, o, ffn_norm, gate, up, down
+        const void* const* w = P.lw + l * 9;   // attn_norm, q, k, v, o, ffn_norm, gate, up, down
         const int qd = P.Hq * HD, kvd = P.Hkv * HD;
         g.w[1] = g.w[2] = nullptr;
         g.n[1] = g.n[2] = 0;
@@ -312,7 +367,7 @@ struct PsState {
     __device__ const unsigned char* stage_wait() {
         const int slot = cons % PS_S;
         volatile int* ab = &sh.abort;
-        if (!*ab && !mbar_wait(&sh.full_bar[slot], (cons / PS_S) & 1)) {
+        if (!*ab && !ps_wait(&sh.full_bar[slot], (cons / PS_S) & 1)) {
             *ab = 1;
             atomicOr(P.err, FAULT_WAIT);
         }
@@ -374,7 +429,7 @@ struct PsState {
         int i = 0;
         for (; have && !*ab; ++i) {
             const int slot = i % PS_S;
-            if (i >= PS_S && !mbar_wait(&sh.empty_bar[slot], ((i / PS_S) - 1) & 1)) {
+            if (i >= PS_S && !ps_wait(&sh.empty_bar[slot], ((i / PS_S) - 1) & 1)) {
                 *ab = 1;
                 atomicOr(P.err, FAULT_WAIT);
                 break;
@@ -393,29 +448,16 @@ struct PsState {
 
     __device__ void grid_arrive(int p) {
         csync();
-        if (tid == 0) {
-            __threadfence();
-            atomicAdd(P.bar + p, 1u);
-        }
+        if (tid == 0) red_release(P.bar + p, 1u);
     }
     __device__ void grid_wait(int p) {
         if (tid == 0) {
             volatile unsigned* gab = P.bar + np + 1;
-            bool ok = false;
-            for (uint32_t i = 0; i < PS_SPIN; ++i) {
-                if (ld_acquire(P.bar + p) >= (unsigned)nc) {
-                    ok = true;
-                    break;
-                }
-                if (*gab) break;
-                __nanosleep(40);
-            }
-            if (!ok) {
+            if (!ps_poll_ge(P.bar + p, (unsigned)nc, gab)) {
                 sh.abort = 1;
                 atomicOr(P.err, FAULT_WAIT);
                 atomicExch(const_cast<unsigned*>(gab), 1u);
             }
-            __threadfence();
         }
         csync();
     }
@@ -477,7 +519,7 @@ __device__ __forceinline__ void ps_gemv(PsState<HD, G, PAGED>& st, const GvGeom&
     const int nst = (row1 - row0 + rps - 1) / rps;
     const int chunk = (PS_RED_ROWS / rps) * rps;   // rows per flush, whole stages
     const size_t row_bytes = (size_t)K * 2;
-    PsShared& sh = st.sh;
+    auto& sh = st.sh;
 
     // the norm gains do not depend on the previous phase: load them before its wait
     uint4 graw[PRO == PRO_RMSNORM ? CPL : 1];
@@ -521,7 +563,7 @@ __device__ __forceinline__ void ps_gemv(PsState<HD, G, PAGED>& st, const GvGeom&
     }
     const bool res_local = EPI == EPI_ADD && (row1 - row0) <= PS_MAX_RES;
     if (EPI == EPI_ADD && res_local)   // read before this phase writes any row; used after a barrier
-        for (int i = tid; i < row1 - row0; i += PS_CT) sh.res[i] = __ldcg(out + row0 + i);
+        for (int i = tid; i < row1 - row0; i += PS_CT) sh.sc.gv.res[i] = __ldcg(out + row0 + i);
 
     unsigned long long best = 0ull;
     bool nonfin = false;
@@ -565,7 +607,7 @@ __device__ __forceinline__ void ps_gemv(PsState<HD, G, PAGED>& st, const GvGeom&
             for (int u = 0; u < RU; ++u) acc[u] += acc2[u];
             int ru;
             const float t = rows_reduce<RU>(acc, lane, ru);
-            if ((lane & (32 / RU - 1)) == 0 && m0 + ru < nr) sh.red[a - c0 + m0 + ru][slice] = t;
+            if ((lane & (32 / RU - 1)) == 0 && m0 + ru < nr) sh.sc.gv.red[a - c0 + m0 + ru][slice] = t;
         }
         st.stage_release();
         // a full chunk (or the phase's last rows): add the slices, write the rows
@@ -578,8 +620,8 @@ __device__ __forceinline__ void ps_gemv(PsState<HD, G, PAGED>& st, const GvGeom&
                     float gs = 0.f, us = 0.f;
 #pragma unroll
                     for (int w = 0; w < PS_SL; ++w) {
-                        gs += sh.red[i][w];
-                        us += sh.red[n + i][w];
+                        gs += sh.sc.gv.red[i][w];
+                        us += sh.sc.gv.red[n + i][w];
                     }
                     out[row0 + i] = gs / (1.0f + expf(-gs)) * us;
                 }
@@ -588,9 +630,9 @@ __device__ __forceinline__ void ps_gemv(PsState<HD, G, PAGED>& st, const GvGeom&
                     const int row = row0 + c0 + i;
                     float t = 0.f;
 #pragma unroll
-                    for (int w = 0; w < PS_SL; ++w) t += sh.red[i][w];
+                    for (int w = 0; w < PS_SL; ++w) t += sh.sc.gv.red[i][w];
                     if (EPI == EPI_ADD) {
-                        out[row] = (res_local ? sh.res[row - row0] : __ldcg(out + row)) + t;
+                        out[row] = (res_local ? sh.sc.gv.res[row - row0] : __ldcg(out + row)) + t;
                     } else {
                         out[row] = t;
                     }
@@ -621,14 +663,19 @@ __device__ __forceinline__ void ps_gemv(PsState<HD, G, PAGED>& st, const GvGeom&
 
 // ---------------- attention phase (tensor cores, as attn_mma.cu) ----------------
 template <int HD, int G, bool PAGED>
-__device__ __forceinline__ void ps_attention(PsState<HD, G, PAGED>& st, int l, float* q_s, float* kn_s, float* vn_s,
-                                             float* wo_s, __nv_bfloat16* qt_s) {
+__device__ __forceinline__ void ps_attention(PsState<HD, G, PAGED>& st, int l) {
     using ST = PsState<HD, G, PAGED>;
     constexpr int PPS = ST::PPS, TILE = ST::TILE;
     constexpr int KPW = PPS / PS_AW, BLK = KPW / 16, KSTEP = HD / 16, DT = HD / 16;
     static_assert(G <= 4, "P^T columns hold G heads' bf16 parts and G remainders");
+    static_assert(KPW >= 16 && KPW % 16 == 0, "each attention warp takes whole 16-key blocks of a stage");
     const PersistParams& P = st.P;
-    PsShared& sh = st.sh;
+    auto& sh = st.sh;
+    float* q_s = sh.sc.at.q;
+    float* kn_s = sh.sc.at.kn;
+    float* vn_s = sh.sc.at.vn;
+    float* wo_s = sh.sc.at.wo;
+    __nv_bfloat16* qt_s = sh.sc.at.qt;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int gq = lane >> 2, tq = lane & 3;
     __nv_bfloat16* Kc = reinterpret_cast<__nv_bfloat16*>(P.kv[2 * l]);
@@ -853,92 +900,86 @@ __device__ __forceinline__ void ps_attention(PsState<HD, G, PAGED>& st, int l, f
             }
         }
         ST::csync();
-        for (int i = tid; i < G * HD; i += PS_CT) {
-            const int h = i / HD, d = i % HD;
+        // per (warp, head) merge factors and the split's (max, sum) per head
+        if (tid < G) {
+            const int h = tid;
             float M = -INFINITY;
 #pragma unroll
             for (int w = 0; w < PS_AW; ++w) M = fmaxf(M, sh.wm[w][h]);
-            float Ls = 0.f, Os = 0.f;
+            float Ls = 0.f;
 #pragma unroll
             for (int w = 0; w < PS_AW; ++w) {
                 const float f = (sh.wm[w][h] == -INFINITY) ? 0.f : expf(sh.wm[w][h] - M);
+                sh.wf[w][h] = f;
                 Ls = fmaf(f, sh.wl[w][h], Ls);
-                Os = fmaf(f, wo_s[(w * G + h) * HD + d], Os);
             }
+            sh.hm[h] = M;
+            sh.hl[h] = Ls;
+        }
+        ST::csync();
+        for (int i = tid; i < G * HD; i += PS_CT) {
+            const int h = i / HD, d = i % HD;
+            float Os = 0.f;
+#pragma unroll
+            for (int w = 0; w < PS_AW; ++w) Os = fmaf(sh.wf[w][h], wo_s[(w * G + h) * HD + d], Os);
             float* pp = P.part + (((size_t)r * P.Hq + g * G + h) * P.nsplit + s) * (HD + 4);
             pp[4 + d] = Os;
             if (d == 0) {
-                pp[0] = M;
-                pp[1] = Ls;
+                pp[0] = sh.hm[h];
+                pp[1] = sh.hl[h];
             }
         }
-        __threadfence();
         ST::csync();
+        // publish the partial; wait until every split of this (row, kv head) has
+        // published (the group's counter grows by nsplit per layer; all CTAs are
+        // resident, and the wait is bounded)
         if (tid == 0) {
-            const unsigned prev = atomicAdd(P.counters + r * P.Hkv + g, 1u);
-            sh.last = prev == (unsigned)P.nsplit - 1u;
+            unsigned* cnt = P.counters + r * P.Hkv + g;
+            red_release(cnt, 1u);
+            const unsigned target = (unsigned)P.nsplit * (unsigned)(l + 1);
+            volatile unsigned* gab = P.bar + st.np + 1;
+            if (!ps_poll_ge(cnt, target, gab)) {
+                sh.abort = 1;
+                atomicOr(P.err, FAULT_WAIT);
+                atomicExch(const_cast<unsigned*>(gab), 1u);
+            }
         }
         ST::csync();
-        if (sh.last) {
-            __threadfence();
-            if (tid == 0) P.counters[r * P.Hkv + g] = 0u;
-            const int NS = P.nsplit;
-            for (int i = tid; i < G * NS; i += PS_CT) {
-                const int h = i / NS, ss = i % NS;
-                const float* pp = P.part + (((size_t)r * P.Hq + g * G + h) * NS + ss) * (HD + 4);
-                sh.cm[h * NS + ss] = __ldcg(pp);
-                sh.cw[h * NS + ss] = __ldcg(pp + 1);
-            }
-            ST::csync();
-            for (int h = warp; h < G; h += PS_CW) {
-                float M = -INFINITY;
-                for (int ss = lane; ss < NS; ss += 32) M = fmaxf(M, sh.cm[h * NS + ss]);
-                M = warp_max(M);
-                float Lsum = 0.f;
-                for (int ss = lane; ss < NS; ss += 32) {
-                    const float mm = sh.cm[h * NS + ss];
-                    Lsum += (mm == -INFINITY) ? 0.f : expf(mm - M) * sh.cw[h * NS + ss];
+        // this split's share of the group's G * HD outputs: every split's
+        // (max, sum, value) requested before any is used
+        {
+            const int NS = P.nsplit, E = G * HD;
+            const int e0 = (int)(((long long)s * E) / NS), e1 = (int)(((long long)(s + 1) * E) / NS);
+            constexpr int CH = 24;   // splits per batch of loads
+            for (int e = e0 + tid; e < e1; e += PS_CT) {
+                const int h = e / HD, d = e % HD;
+                const float* base = P.part + (((size_t)r * P.Hq + g * G + h) * NS) * (HD + 4);
+                float M = -INFINITY, Lsum = 0.f, acc = 0.f;
+                for (int s0 = 0; s0 < NS; s0 += CH) {
+                    float mv[CH], lv[CH], ov[CH];
+#pragma unroll
+                    for (int j = 0; j < CH; ++j) {
+                        const bool in = s0 + j < NS;
+                        const float* pj = base + (size_t)(in ? s0 + j : 0) * (HD + 4);
+                        mv[j] = in ? __ldcg(pj) : -INFINITY;
+                        lv[j] = in ? __ldcg(pj + 1) : 0.f;
+                        ov[j] = in ? __ldcg(pj + 4 + d) : 0.f;
+                    }
+                    float Mc = M;
+#pragma unroll
+                    for (int j = 0; j < CH; ++j) Mc = fmaxf(Mc, mv[j]);
+                    const float resc = (M == -INFINITY) ? 0.f : expf(M - Mc);
+                    Lsum *= resc;
+                    acc *= resc;
+#pragma unroll
+                    for (int j = 0; j < CH; ++j) {
+                        const float f = (mv[j] == -INFINITY) ? 0.f : expf(mv[j] - Mc);
+                        Lsum = fmaf(f, lv[j], Lsum);
+                        acc = fmaf(f, ov[j], acc);
+                    }
+                    M = Mc;
                 }
-                Lsum = warp_sum(Lsum);
-                for (int ss = lane; ss < NS; ss += 32) {
-                    const float mm = sh.cm[h * NS + ss];
-                    sh.cw[h * NS + ss] = (mm == -INFINITY) ? 0.f : expf(mm - M) / Lsum;
-                }
-            }
-            ST::csync();
-            // every partial this thread needs is requested before any is used
-            constexpr int PER = (G * HD + PS_CT - 1) / PS_CT;   // outputs per thread
-            constexpr int CH = 16;                              // splits per batch of loads
-            float acc[PER];
-#pragma unroll
-            for (int q = 0; q < PER; ++q) acc[q] = 0.f;
-            for (int s0 = 0; s0 < NS; s0 += CH) {
-                float v[PER][CH];
-#pragma unroll
-                for (int q = 0; q < PER; ++q) {
-                    const int i = tid + q * PS_CT;
-                    const int h = min(i, G * HD - 1) / HD, d = min(i, G * HD - 1) % HD;
-                    const float* base = P.part + (((size_t)r * P.Hq + g * G + h) * NS) * (HD + 4) + 4 + d;
-#pragma unroll
-                    for (int j = 0; j < CH; ++j)
-                        v[q][j] = s0 + j < NS ? __ldcg(base + (size_t)(s0 + j) * (HD + 4)) : 0.f;
-                }
-#pragma unroll
-                for (int q = 0; q < PER; ++q) {
-                    const int h = min(tid + q * PS_CT, G * HD - 1) / HD;
-#pragma unroll
-                    for (int j = 0; j < CH; ++j)
-                        if (s0 + j < NS) acc[q] = fmaf(sh.cw[h * NS + s0 + j], v[q][j], acc[q]);
-                }
-            }
-#pragma unroll
-            for (int q = 0; q < PER; ++q) {
-                const int i = tid + q * PS_CT;
-                if (i < G * HD) {
-                    const int h = i / HD, d = i % HD;
-                    const float out = acc[q];
-                    P.attn[(size_t)r * P.Hq * HD + (size_t)(g * G + h) * HD + d] = out;
-                }
+                P.attn[(size_t)r * P.Hq * HD + (size_t)(g * G + h) * HD + d] = acc / Lsum;
             }
         }
         ST::csync();
@@ -950,14 +991,10 @@ __global__ void __launch_bounds__(PS_THREADS, 1) k_persist(const __grid_constant
     extern __shared__ __align__(1024) unsigned char ps_raw[];
     unsigned char* ring =
         reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(ps_raw) + 1023) & ~(uintptr_t)1023);
-    __shared__ PsShared sh;
-    __shared__ float q_s[G * HD], kn_s[HD], vn_s[HD];
-    __shared__ float wo_s[PS_AW * G * HD];
-    __shared__ __align__(16) __nv_bfloat16 qt_s[16 * (HD + 8)];
+    __shared__ PsShared<HD, G> sh;
     using ST = PsState<HD, G, PAGED>;
     const int tid = threadIdx.x;
 
-    for (int i = tid; i < P.L * 9; i += PS_THREADS) sh.wtab[i] = P.lw[i];
     if (tid == 0) {
         for (int s = 0; s < PS_S; ++s) {
             mbar_init(&sh.full_bar[s], 1);
@@ -1012,7 +1049,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) k_persist(const __grid_constant
                     }
                 }
             } else if (k == PK_ATTN) {
-                ps_attention<HD, G, PAGED>(st, st.layer(p), q_s, kn_s, vn_s, wo_s, qt_s);
+                ps_attention<HD, G, PAGED>(st, st.layer(p));
             } else {
                 GvGeom g;
                 const int l = k == PK_HEAD ? 0 : st.layer(p);
@@ -1021,14 +1058,14 @@ __global__ void __launch_bounds__(PS_THREADS, 1) k_persist(const __grid_constant
                 switch (k) {
                     case PK_QKV:
                         ps_gemv<CPL_D, PRO_RMSNORM, EPI_STORE>(st, g, P.x,
-                            reinterpret_cast<const __nv_bfloat16*>(sh.wtab[l * 9 + 0]), P.qkv, p);
+                            reinterpret_cast<const __nv_bfloat16*>(P.lw[l * 9 + 0]), P.qkv, p);
                         break;
                     case PK_O:
                         ps_gemv<CPL_D, PRO_PLAIN, EPI_ADD>(st, g, P.attn, w9, P.x, p);
                         break;
                     case PK_GU:
                         ps_gemv<CPL_D, PRO_RMSNORM, EPI_SWIGLU_PAIR>(st, g, P.x,
-                            reinterpret_cast<const __nv_bfloat16*>(sh.wtab[l * 9 + 5]), P.gu, p);
+                            reinterpret_cast<const __nv_bfloat16*>(P.lw[l * 9 + 5]), P.gu, p);
                         break;
                     case PK_DOWN:
                         ps_gemv<CPL_F, PRO_PLAIN, EPI_ADD>(st, g, P.gu, w9, P.x, p);
@@ -1053,6 +1090,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) k_persist(const __grid_constant
         const unsigned prev = atomicAdd(P.bar + np, 1u);
         if (prev == (unsigned)gridDim.x - 1u) {
             for (int p = 0; p <= np + 1; ++p) P.bar[p] = 0u;
+            for (int i = 0; i < P.R * P.Hkv; ++i) P.counters[i] = 0u;
             __threadfence();
         }
     }
@@ -1076,7 +1114,7 @@ static int cpl_of(int K) { return (K / (PS_SL * 8) + 31) / 32; }
 
 cudaError_t persist_plan(PersistPlan* plan, int num_sms) {
     PersistParams& p = plan->p;
-    if (p.R != 1 || p.L > PS_MAX_L) return cudaErrorNotSupported;
+    if (p.R != 1) return cudaErrorNotSupported;
     if (p.Hq * p.hd != p.d) return cudaErrorNotSupported;   // O-proj uses the d-column variant
     if (p.d % (PS_SL * 8 * 32) || p.F % (PS_SL * 8 * 32)) return cudaErrorNotSupported;
     const int cd = cpl_of(p.d), cf = cpl_of(p.F);
@@ -1109,15 +1147,16 @@ cudaError_t persist_plan(PersistPlan* plan, int num_sms) {
         L = (L + half - 1) / half * half;
         if (p.paged) L = (L + p.page - 1) / p.page * p.page;
         const int ns = (p.cap + L - 1) / L;
-        if (ns > PS_MAX_NS) continue;
-        const long long per_cta = ((long long)units0 * ns + num_sms - 1) / num_sms;
-        const long long cost = per_cta * L + 16LL * ns;
+        // one unit per CTA at most: the splits of a group wait for each other
+        if (ns > PS_MAX_NS || (long long)units0 * ns > num_sms) continue;
+        const long long cost = (long long)L + 16LL * ns;
         if (best < 0 || cost < best) {
             best = cost;
             bl = L;
             bn = ns;
         }
     }
+    if (bn == 0) return cudaErrorNotSupported;
     p.split_len = bl;
     p.nsplit = bn;
     p.pf = 0;
