@@ -30,7 +30,9 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "decode tokens/s and µs/token at 1 GB300; achieved HBM GB/s vs roofline"
-PROFILE = os.path.join(ROOT, "profiles", "gemv_gate_up_8b.md")
+# committed ncu summaries: DRAM bytes per launch of the roofline kernel, valid while its source is unchanged
+PROFILES = {"persistent": (os.path.join(ROOT, "profiles", "persist_step_8b.md"), "persist.cu"),
+            "graph": (os.path.join(ROOT, "profiles", "gemv_gate_up_8b.md"), "gemv_impl.cuh")}
 
 
 def _peaks():
@@ -107,18 +109,19 @@ class Clocks:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def _traffic_from_profile():
-    """DRAM bytes per launch of the dominant kernel from the committed ncu summary,
+def _traffic_from_profile(strategy):
+    """DRAM bytes per launch of the roofline kernel from the committed ncu summary,
     or None if the summary is missing or the kernel source changed since."""
+    path, src_name = PROFILES[strategy]
     try:
-        txt = open(PROFILE).read()
+        txt = open(path).read()
     except OSError:
         return None
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
-    h = re.search(r"gemv_source_sha256:\s*([0-9a-f]+)", txt)
+    h = re.search(r"source_sha256:\s*([0-9a-f]+)", txt)
     if not m or not h:
         return None
-    src = open(os.path.join(ROOT, "graph_replay_gb300", "csrc", "gemv.cu"), "rb").read()
+    src = open(os.path.join(ROOT, "graph_replay_gb300", "csrc", src_name), "rb").read()
     if hashlib.sha256(src).hexdigest() != h.group(1):
         return None
     return float(m.group(1))
@@ -258,7 +261,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     k_us = k0.elapsed_time(k1) * 1e3 / len(idx)
     k_gbs = kbytes / (k_us * 1e-6) / 1e9
-    traffic = _traffic_from_profile() if (wl.name == "8b" and not persistent) else None
+    traffic = _traffic_from_profile(args.strategy) if wl.name == "8b" else None
 
     step_bytes = wl.step_bytes()
     step_gbs = step_bytes / (ms_step * 1e-3) / 1e9
@@ -351,7 +354,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--strategy", default="graph", choices=["graph", "persistent"],
+    ap.add_argument("--strategy", default="persistent", choices=["graph", "persistent"],
                     help="graph: the step's kernel sequence in one CUDA graph; persistent: one whole-step kernel")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (reduced case for profilers)")
     ap.add_argument("--vocab", type=int, default=0, help="override the vocabulary (reduced case for profilers)")
