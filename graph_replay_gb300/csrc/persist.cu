@@ -422,24 +422,40 @@ struct PsState {
         PsStage s;
         volatile int* ab = &sh.abort;
         bool have = next(c, s);
-        // second cursor: L2 prefetches of the next P.pf stages, issued before their slots free
+        // second cursor: while the producer waits for a slot (the compute warps
+        // are behind, e.g. at a phase dependency), it prefetches the stages after
+        // the pending one into L2, up to P.pf ahead, so HBM keeps streaming
         PsCursor f = c;
         PsStage sf;
-        int fi = 1;   // next stage index of f
+        int fi = 1;   // stage index next(f) yields
         int i = 0;
         for (; have && !*ab; ++i) {
             const int slot = i % PS_S;
-            if (i >= PS_S && !ps_wait(&sh.empty_bar[slot], ((i / PS_S) - 1) & 1)) {
-                *ab = 1;
-                atomicOr(P.err, FAULT_WAIT);
-                break;
+            if (i >= PS_S) {
+                const uint32_t par = ((i / PS_S) - 1) & 1;
+                if (fi <= i) {   // f fell behind the ring: restart it after stage i
+                    f = c;
+                    fi = i + 1;
+                }
+                bool ok = false;
+                for (uint32_t it = 0; it < MBAR_POLLS; ++it) {
+                    if (mbar_try_wait(&sh.empty_bar[slot], par)) {
+                        ok = true;
+                        break;
+                    }
+                    if (P.pf > 0 && (it & 3u) == 3u && fi <= i + P.pf && next(f, sf)) {
+                        prefetch(sf);
+                        ++fi;
+                    }
+                }
+                if (!ok) {
+                    *ab = 1;
+                    atomicOr(P.err, FAULT_WAIT);
+                    break;
+                }
             }
             issue(s, slot);
             have = next(c, s);
-            while (fi <= i + P.pf && next(f, sf)) {   // stages i + 1 .. i + pf, ahead of their slots
-                prefetch(sf);
-                ++fi;
-            }
         }
         // no copy may still be landing when the CTA exits (after an abort some were never consumed)
         for (int j = max(0, i - PS_S); j < i; ++j)
