@@ -172,13 +172,17 @@ struct PsState {
     unsigned char* ring;
     int cta, nc, np, tid;
     int cons;   // stages consumed (uniform over the CTA)
+    // the trace buffer if tracing is on for this launch, else null: the enable
+    // word is read once, so a disabled trace costs no L2 round trips per phase
+    unsigned long long* trace;
 
     static constexpr int PPS = PS_SLOT / (2 * HD * 2);   // keys per full attention stage
     static constexpr int TILE = PPS * HD * 2;            // bytes of the K (or V) tile
     static constexpr int SUB = HD / 64;
 
-    __device__ PsState(const PersistParams& p, PsShared<HD, G>& s, unsigned char* r)
-        : P(p), sh(s), ring(r), cta(blockIdx.x), nc(gridDim.x), np(5 * p.L + 2), tid(threadIdx.x), cons(0) {}
+    __device__ PsState(const PersistParams& p, PsShared<HD, G>& s, unsigned char* r, bool trace_on)
+        : P(p), sh(s), ring(r), cta(blockIdx.x), nc(gridDim.x), np(5 * p.L + 2), tid(threadIdx.x), cons(0),
+          trace(trace_on ? p.trace : nullptr) {}
 
     __device__ int kind(int p) const { return p == 0 ? PK_EMBED : (p == np - 1 ? PK_HEAD : 1 + (p - 1) % 5); }
     __device__ int layer(int p) const { return (p - 1) / 5; }
@@ -544,7 +548,7 @@ __device__ __forceinline__ void ps_gemv(PsState<HD, G, PAGED>& st, const GvGeom&
         for (int j = 0; j < CPL; ++j) graw[j] = *reinterpret_cast<const uint4*>(gain + (vbase + lane + 32 * j) * VEC);
     }
     st.grid_wait(phase - 1);
-    if (tid == 0) trace_stamp(st.P.trace, phase, 1);
+    if (tid == 0 && st.trace) trace_stamp(st.trace, phase, 1);
 
     // prologue: this lane's activations (its slice columns), in registers; the
     // slices of the compute warps cover K exactly, so they also give the norm
@@ -1020,7 +1024,8 @@ __global__ void __launch_bounds__(PS_THREADS, 1) k_persist(const __grid_constant
         mbar_fence_init();
     }
     __syncthreads();
-    ST st(P, sh, ring);
+    const bool trace_on = P.trace && *reinterpret_cast<const volatile unsigned long long*>(P.trace) != 0ull;
+    ST st(P, sh, ring, trace_on);
     const int np = st.np;
 
     if (tid >= PS_CT) {
@@ -1031,11 +1036,11 @@ __global__ void __launch_bounds__(PS_THREADS, 1) k_persist(const __grid_constant
     } else {
         for (int p = 0; p < np; ++p) {
             const int k = st.kind(p);
-            if (tid == 0) trace_stamp(P.trace, p, 0);
+            if (tid == 0 && st.trace) trace_stamp(st.trace, p, 0);
             const bool gemv = k != PK_EMBED && k != PK_ATTN;   // GEMV phases wait inside (after their gain loads)
             if (!gemv) {
                 if (p > 0) st.grid_wait(p - 1);
-                if (tid == 0) trace_stamp(P.trace, p, 1);
+                if (tid == 0 && st.trace) trace_stamp(st.trace, p, 1);
             }
             if (k == PK_EMBED) {
                 if (st.cta == 0) {
@@ -1093,9 +1098,9 @@ __global__ void __launch_bounds__(PS_THREADS, 1) k_persist(const __grid_constant
                 }
             }
             st.grid_arrive(p);
-            if (tid == 0) {
-                trace_stamp(P.trace, p, 2);
-                trace_stamp(P.trace, p, 3);
+            if (tid == 0 && st.trace) {
+                trace_stamp(st.trace, p, 2);
+                trace_stamp(st.trace, p, 3);
             }
         }
     }
