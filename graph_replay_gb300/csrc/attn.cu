@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(AT_THREADS) k_attn(const AttnParams p) {
 
     if (warp == AT_CW) {
         // ---------------- producer: K and V tiles of this split ----------------
-        if (lane == 1) trace_stamp(p.trace, p.trace_id, 0);
+        if (lane == 1) trace_mark(trace_if_on(p.trace), p.trace_id, 0);
         if (lane == 0) {
             int issued = 0;
             for (int t = 0; t < nst; ++t) {
@@ -144,7 +144,11 @@ __global__ void __launch_bounds__(AT_THREADS) k_attn(const AttnParams p) {
 
     // ---------------- consumers ----------------
     pdl_wait();
-    if (tid == 0) trace_stamp(p.trace, p.trace_id, 1);
+    unsigned long long* tr = nullptr;   // trace buffer if tracing is on (thread 0)
+    if (tid == 0) {
+        tr = trace_if_on(p.trace);
+        trace_mark(tr, p.trace_id, 1);
+    }
     int pos = p.pos[r];
     pos = min(max(pos, 0), p.cap - 1);   // an out-of-range pos was flagged by the embedding kernel
     const float* qrow = p.qkv + (size_t)r * p.qkv_stride;
@@ -346,7 +350,7 @@ __global__ void __launch_bounds__(AT_THREADS) k_attn(const AttnParams p) {
         last_s = (prev == (unsigned)p.nsplit - 1u);
     }
     named_sync(1, AT_CT);
-    if (tid == 0) trace_stamp(p.trace, p.trace_id, 2);
+    if (tid == 0) trace_mark(tr, p.trace_id, 2);
     if (!last_s) return;
     __threadfence();
     if (tid == 0) p.counters[r * p.Hkv + g] = 0u;   // ready for the next step
@@ -390,7 +394,7 @@ __global__ void __launch_bounds__(AT_THREADS) k_attn(const AttnParams p) {
         p.out[(size_t)r * p.Hq * HD + (size_t)(g * G + h) * HD + d] = acc;
     }
     named_sync(1, AT_CT);
-    if (tid == 0) trace_stamp(p.trace, p.trace_id, 3);
+    if (tid == 0) trace_mark(tr, p.trace_id, 3);
 }
 
 // ---------------- host side ----------------

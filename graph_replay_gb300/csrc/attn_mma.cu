@@ -121,17 +121,19 @@ __global__ void __launch_bounds__(AM_THREADS, 2) k_attn_mma(const __grid_constan
         }
     };
     int issued = 0;
+    unsigned long long* tr = nullptr;   // trace buffer if tracing is on (thread 0)
     if (tid == 0) {
         for (int i = 0; i < S; ++i) mbar_init(&full_bar[i], 1);
         abort_s = 0;
         mbar_fence_init();
         for (; issued < min(S, nst); ++issued) issue(issued);
-        trace_stamp(p.trace, p.trace_id, 0);   // after the copies: the trace read is a global load
+        tr = trace_if_on(p.trace);   // after the copies: the enable word is a global load
+        trace_mark(tr, p.trace_id, 0);
     }
     __syncthreads();
 
     pdl_wait();
-    if (tid == 0) trace_stamp(p.trace, p.trace_id, 1);
+    if (tid == 0) trace_mark(tr, p.trace_id, 1);
     int pos = p.pos[r];
     pos = min(max(pos, 0), p.cap - 1);   // an out-of-range pos was flagged by the embedding kernel
     const float* qrow = p.qkv + (size_t)r * p.qkv_stride;
@@ -364,7 +366,7 @@ __global__ void __launch_bounds__(AM_THREADS, 2) k_attn_mma(const __grid_constan
     if (tid == 0) {
         const unsigned prev = atomicAdd(p.counters + r * p.Hkv + g, 1u);
         last_s = (prev == (unsigned)p.nsplit - 1u);
-        trace_stamp(p.trace, p.trace_id, 2);
+        trace_mark(tr, p.trace_id, 2);
     }
     __syncthreads();
     if (!last_s) return;
@@ -409,7 +411,7 @@ __global__ void __launch_bounds__(AM_THREADS, 2) k_attn_mma(const __grid_constan
         p.out[(size_t)r * p.Hq * HD + (size_t)(g * G + h) * HD + d] = acc;
     }
     __syncthreads();
-    if (tid == 0) trace_stamp(p.trace, p.trace_id, 3);
+    if (tid == 0) trace_mark(tr, p.trace_id, 3);
 }
 
 // ---------------- host side ----------------

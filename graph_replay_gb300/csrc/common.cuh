@@ -29,9 +29,16 @@ __device__ __forceinline__ unsigned long long gtimer() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
-__device__ __forceinline__ void trace_stamp(unsigned long long* tr, int id, int slot) {
-    if (tr && *reinterpret_cast<volatile unsigned long long*>(tr)) {
-        unsigned long long* w = tr + 1 + 4 * id + slot;
+// The trace buffer if this launch records a trace, else null: one global load
+// of the enable word per thread that stamps, so a disabled trace costs no
+// further round trips.
+__device__ __forceinline__ unsigned long long* trace_if_on(unsigned long long* tr) {
+    return (tr && *reinterpret_cast<volatile unsigned long long*>(tr)) ? tr : nullptr;
+}
+// stamp into a buffer that trace_if_on returned (nothing on null)
+__device__ __forceinline__ void trace_mark(unsigned long long* on, int id, int slot) {
+    if (on) {
+        unsigned long long* w = on + 1 + 4 * id + slot;
         const unsigned long long t = gtimer();
         if (slot == 0 || slot == 2) atomicMin(w, t);
         else atomicMax(w, t);

@@ -104,20 +104,22 @@ __global__ void __launch_bounds__(GV_THREADS, 2) k_gemv(const GemvParams p) {
             r = e;
         }
     };
-    int issued = 0;   // meaningful in thread 0
+    int issued = 0;                  // meaningful in thread 0
+    unsigned long long* tr = nullptr;   // trace buffer if tracing is on (thread 0)
     if (tid == 0) {
         for (int s = 0; s < S; ++s) mbar_init(&full_bar[s], 1);
         abort_s = 0;
         mbar_fence_init();
         // the first ring fill does not depend on the previous kernel
         for (; issued < min(S, nst); ++issued) issue(issued);
-        trace_stamp(p.trace, p.trace_id, 0);   // after the copies: the trace read is a global load
+        tr = trace_if_on(p.trace);   // after the copies: the enable word is a global load
+        trace_mark(tr, p.trace_id, 0);
     }
     __syncthreads();
 
     // ---------------- consumers ----------------
     pdl_wait();
-    if (tid == 0) trace_stamp(p.trace, p.trace_id, 1);
+    if (tid == 0) trace_mark(tr, p.trace_id, 1);
     const int SWV = K / (GV_SL * VEC);   // 16-byte vectors in one warp's K-slice
     const int slice = warp % GV_SL, grp = warp / GV_SL;
     const int vbase = slice * SWV;
@@ -351,8 +353,8 @@ __global__ void __launch_bounds__(GV_THREADS, 2) k_gemv(const GemvParams p) {
         // can an issued stage be unconsumed)
         for (int k = max(0, issued - S); k < issued; ++k)
             if (!mbar_wait(&full_bar[k % S], (k / S) & 1)) atomicOr(p.err, FAULT_WAIT);
-        trace_stamp(p.trace, p.trace_id, 2);
-        trace_stamp(p.trace, p.trace_id, 3);
+        trace_mark(tr, p.trace_id, 2);
+        trace_mark(tr, p.trace_id, 3);
     }
     if (EPI == EPI_LOGITS && warp == 0) {
 #pragma unroll

@@ -16,7 +16,11 @@ namespace gd {
 template <typename WT>
 __global__ void __launch_bounds__(256) k_embed(const EmbedParams p) {
     const int tid = threadIdx.x;
-    if (tid == 0) trace_stamp(p.trace, p.trace_id, 0);
+    unsigned long long* tr = nullptr;   // trace buffer if tracing is on (thread 0)
+    if (tid == 0) {
+        tr = trace_if_on(p.trace);
+        trace_mark(tr, p.trace_id, 0);
+    }
     if (tid == 0) *p.err = 0u;
     if (tid < p.R) {
         p.amax[tid] = 0ull;
@@ -46,9 +50,9 @@ __global__ void __launch_bounds__(256) k_embed(const EmbedParams p) {
     }
     __syncthreads();
     if (tid == 0) {
-        trace_stamp(p.trace, p.trace_id, 1);
-        trace_stamp(p.trace, p.trace_id, 2);
-        trace_stamp(p.trace, p.trace_id, 3);
+        trace_mark(tr, p.trace_id, 1);
+        trace_mark(tr, p.trace_id, 2);
+        trace_mark(tr, p.trace_id, 3);
     }
 }
 

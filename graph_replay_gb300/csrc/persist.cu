@@ -548,7 +548,7 @@ __device__ __forceinline__ void ps_gemv(PsState<HD, G, PAGED>& st, const GvGeom&
         for (int j = 0; j < CPL; ++j) graw[j] = *reinterpret_cast<const uint4*>(gain + (vbase + lane + 32 * j) * VEC);
     }
     st.grid_wait(phase - 1);
-    if (tid == 0 && st.trace) trace_stamp(st.trace, phase, 1);
+    if (tid == 0 && st.trace) trace_mark(st.trace, phase, 1);
 
     // prologue: this lane's activations (its slice columns), in registers; the
     // slices of the compute warps cover K exactly, so they also give the norm
@@ -1024,8 +1024,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) k_persist(const __grid_constant
         mbar_fence_init();
     }
     __syncthreads();
-    const bool trace_on = P.trace && *reinterpret_cast<const volatile unsigned long long*>(P.trace) != 0ull;
-    ST st(P, sh, ring, trace_on);
+    ST st(P, sh, ring, trace_if_on(P.trace) != nullptr);
     const int np = st.np;
 
     if (tid >= PS_CT) {
@@ -1036,11 +1035,11 @@ __global__ void __launch_bounds__(PS_THREADS, 1) k_persist(const __grid_constant
     } else {
         for (int p = 0; p < np; ++p) {
             const int k = st.kind(p);
-            if (tid == 0 && st.trace) trace_stamp(st.trace, p, 0);
+            if (tid == 0 && st.trace) trace_mark(st.trace, p, 0);
             const bool gemv = k != PK_EMBED && k != PK_ATTN;   // GEMV phases wait inside (after their gain loads)
             if (!gemv) {
                 if (p > 0) st.grid_wait(p - 1);
-                if (tid == 0 && st.trace) trace_stamp(st.trace, p, 1);
+                if (tid == 0 && st.trace) trace_mark(st.trace, p, 1);
             }
             if (k == PK_EMBED) {
                 if (st.cta == 0) {
@@ -1099,8 +1098,8 @@ __global__ void __launch_bounds__(PS_THREADS, 1) k_persist(const __grid_constant
             }
             st.grid_arrive(p);
             if (tid == 0 && st.trace) {
-                trace_stamp(st.trace, p, 2);
-                trace_stamp(st.trace, p, 3);
+                trace_mark(st.trace, p, 2);
+                trace_mark(st.trace, p, 3);
             }
         }
     }
