@@ -526,10 +526,17 @@ int dec_capture(dec_handle* h, int32_t cap, int32_t rows, int32_t kv_layout, int
                              &h->d_status->err, h->d_status->amax, h->d_status->nonfinite, h->d_trace, 0};
     h->gemv.clear();
     h->attn.clear();
+    // Projections of 2..8 bf16 rows are dense contractions: tensor-core GEMV
+    // (GRAPHDEC_GEMV=simd keeps the CUDA-core GEMV at every row count).  Its
+    // gate/up kernel applies SwiGLU in the epilogue, so the down projection
+    // reads silu(gate) * up from the first F columns of the gate/up buffer.
+    const char* gemv_env = getenv("GRAPHDEC_GEMV");
+    const bool tc = wt == W_BF16 && rows >= 2 && !(gemv_env && strcmp(gemv_env, "simd") == 0);
     auto mk = [&](int pro, int epi, const void* w0, int n0, const void* w1, int n1, const void* w2, int n2, int K,
                   const float* act, int act_stride, const void* gain, float* out, int out_stride) {
         GemvPlan pl{};
         pl.wtype = wt;
+        pl.tc = tc ? 1 : 0;
         pl.pro = pro;
         pl.epi = epi;
         GemvParams& p = pl.p;
@@ -556,8 +563,17 @@ int dec_capture(dec_handle* h, int32_t cap, int32_t rows, int32_t kv_layout, int
                              h->d_qkv, qkv_stride));
         h->gemv.push_back(mk(PRO_PLAIN, EPI_ADD, w[4], d, nullptr, 0, nullptr, 0, Hq * hd, h->d_attn, Hq * hd, nullptr,
                              h->d_x, d));
-        h->gemv.push_back(mk(PRO_RMSNORM, EPI_STORE, w[6], F, w[7], F, nullptr, 0, d, h->d_x, d, w[5], h->d_gu, 2 * F));
-        h->gemv.push_back(mk(PRO_SWIGLU, EPI_ADD, w[8], d, nullptr, 0, nullptr, 0, F, h->d_gu, 2 * F, nullptr, h->d_x, d));
+        if (tc) {
+            h->gemv.push_back(mk(PRO_RMSNORM, EPI_SWIGLU, w[6], F, w[7], F, nullptr, 0, d, h->d_x, d, w[5], h->d_gu,
+                                 2 * F));
+            h->gemv.push_back(mk(PRO_PLAIN, EPI_ADD, w[8], d, nullptr, 0, nullptr, 0, F, h->d_gu, 2 * F, nullptr,
+                                 h->d_x, d));
+        } else {
+            h->gemv.push_back(mk(PRO_RMSNORM, EPI_STORE, w[6], F, w[7], F, nullptr, 0, d, h->d_x, d, w[5], h->d_gu,
+                                 2 * F));
+            h->gemv.push_back(mk(PRO_SWIGLU, EPI_ADD, w[8], d, nullptr, 0, nullptr, 0, F, h->d_gu, 2 * F, nullptr,
+                                 h->d_x, d));
+        }
         AttnPlan ap{};
         ap.kvtype = c.kv_dtype == DEC_DTYPE_BF16 ? W_BF16 : W_F32;
         ap.paged = kv_layout == DEC_KV_PAGED;
@@ -889,7 +905,8 @@ int dec_launch_kernel(dec_handle* h, int32_t index, int32_t pdl, int64_t* bytes)
             e = gemv_launch(g, h->stream, pdl != 0);
             const int64_t act_in = g.pro == PRO_SWIGLU ? 2 * g.p.K : g.p.K;
             const int64_t out_rw = g.epi == EPI_ADD ? 8 : 4;
-            b = (int64_t)g.p.N * g.p.K * wes + R * act_in * 4 + R * (int64_t)g.p.N * out_rw +
+            const int64_t n_out = g.epi == EPI_SWIGLU ? g.p.N / 2 : g.p.N;
+            b = (int64_t)g.p.N * g.p.K * wes + R * act_in * 4 + R * n_out * out_rw +
                 (g.pro == PRO_RMSNORM ? g.p.K * wes : 0);
         }
     }

@@ -7,6 +7,8 @@ namespace gd {
 
 const void* gemv_kernel_bf16(int nr, int cpl, int pro, int epi);
 const void* gemv_kernel_f32(int nr, int cpl, int pro, int epi);
+const void* gemv_tc_kernel(int pro, int epi);
+cudaError_t gemv_tc_plan(GemvPlan* plan, int num_sms);
 
 namespace {
 // mirrors gemv_impl.cuh
@@ -18,6 +20,7 @@ constexpr int MAX_S = 6;
 constexpr int MAX_RPS = 32;
 
 const void* pick(const GemvPlan& pl) {
+    if (pl.tc) return gemv_tc_kernel(pl.pro, pl.epi);
     return pl.wtype == W_BF16 ? gemv_kernel_bf16(pl.nr, pl.cpl, pl.pro, pl.epi)
                               : gemv_kernel_f32(pl.nr, pl.cpl, pl.pro, pl.epi);
 }
@@ -40,6 +43,7 @@ int cpl_for(int need, int nr, int wtype) {
 }  // namespace
 
 cudaError_t gemv_plan(GemvPlan* plan, int num_sms) {
+    if (plan->tc) return gemv_tc_plan(plan, num_sms);
     GemvParams& p = plan->p;
     const int vec = plan->wtype == W_BF16 ? 8 : 4;
     const int es = plan->wtype == W_BF16 ? 2 : 4;

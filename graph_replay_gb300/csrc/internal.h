@@ -32,7 +32,9 @@ enum WType { W_F32 = 0, W_BF16 = 1 };
 //   PRO_SWIGLU  a = silu(act[:, :K]) * act[:, K:2K]
 enum Prologue { PRO_PLAIN = 0, PRO_RMSNORM = 1, PRO_SWIGLU = 2 };
 // Epilogue: store, add into out (residual), or store logits + greedy argmax.
-enum Epilogue { EPI_STORE = 0, EPI_ADD = 1, EPI_LOGITS = 2 };
+// EPI_SWIGLU (tensor-core GEMV only): segments 0 and 1 are gate and up with the
+// same row count F, and out[r, n] = silu(gate_n . a_r) * (up_n . a_r), n < F.
+enum Epilogue { EPI_STORE = 0, EPI_ADD = 1, EPI_LOGITS = 2, EPI_SWIGLU = 3 };
 
 struct GemvParams {
     const void* w[3];
@@ -57,6 +59,7 @@ struct GemvParams {
 
 struct GemvPlan {
     int wtype, pro, epi, nr, cpl;
+    int tc;                // 1: tensor-core GEMV (gemv_tc.cu, bf16 weights, 1..8 rows)
     int grid, block;
     size_t smem;
     GemvParams p;
