@@ -465,6 +465,8 @@ cudaError_t attn_plan(AttnPlan* plan, int num_sms) {
         if ((long long)((size_t)S * AT_STAGE + extra) > per_cta) return 0;
         return S;
     };
+    // the occupancy queries below see the dynamic shared-memory cap: raise it first
+    if (cudaError_t e0 = raise_smem_cap(fn)) return e0;
     int kmax = 1;
     for (int k = 2; k <= 3; ++k) {
         const int S = ring_stages(k, max_ns);

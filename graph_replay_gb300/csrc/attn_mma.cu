@@ -485,6 +485,8 @@ cudaError_t attn_mma_plan(AttnPlan* plan, int num_sms) {
     if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess) return e;
     cudaFuncAttributes fa;
     if ((e = cudaFuncGetAttributes(&fa, fn)) != cudaSuccess) return e;
+    // the occupancy queries below see the dynamic shared-memory cap: raise it first
+    if ((e = raise_smem_cap(fn)) != cudaSuccess) return e;
     const int units = p.R * p.Hkv;
     const int max_ns = (p.cap + pps - 1) / pps;
     auto extra = [&](int ns) {
@@ -520,7 +522,10 @@ cudaError_t attn_mma_plan(AttnPlan* plan, int num_sms) {
         if (per_sm > kmax && want > 1) continue;
         // the final merge stages [G][ns][hd + 4] floats in a ring of >= 2 stages
         if ((size_t)plan->group * ns * (p.hd + 4) * sizeof(float) > 2 * (size_t)AM_STAGE && want > 1) continue;
-        const long long cost = per_sm * Ls + 64;   // + a small per-split merge cost
+        // one CTA streams well below an SM's share of HBM bandwidth, so CTAs
+        // sharing an SM run side by side: the time is the split length
+        // (+ a small per-split merge cost)
+        const long long cost = Ls + 64;
         if (best_cost < 0 || cost < best_cost) {
             best_cost = cost;
             best_L = Ls;

@@ -33,6 +33,7 @@ thread_local std::string g_init_msg;   // message of the last failed dec_init on
 
 constexpr int ST_READY = 0, ST_NEEDS_RESET = 1, ST_POISONED = 2;
 constexpr int MAX_ROWS = 8;
+constexpr int CHAIN_MAX = DEC_CHAIN_MAX_STEPS;   // steps one dec_chain call records
 constexpr size_t ALIGN = 256;
 
 // per-step status block read back after every step (one copy)
@@ -49,8 +50,8 @@ int es_of(int dtype) { return dtype == DEC_DTYPE_BF16 ? 2 : 4; }
 
 // Offsets of every buffer of a capture inside one workspace.
 struct WsLayout {
-    size_t status, slots, slot_map, counters, trace, ptabs, tmaps, gbar, x, qkv, attn, gu, logits, part, rope, kv,
-        kv_layer, total;
+    size_t status, slots, slot_map, counters, trace, ptabs, tmaps, gbar, x, qkv, attn, gu, logits, part, gpart, gcnt,
+        chain, rope, kv, kv_layer, total;
 };
 
 // kernels recorded per step: embedding, 5 per layer, head
@@ -77,6 +78,19 @@ bool compute_layout(const dec_config& c, int cap, int R, int layout, int page, i
     L->gu = take((size_t)R * 2 * F * 4);
     L->logits = take((size_t)R * V * 4);
     L->part = take(attn_part_floats(R, (int)Hq, (int)hd, (int)max_splits) * 4);
+    // split-K partial sums of the tensor-core GEMV (bf16, 2..8 rows): the largest projection's need
+    size_t gp = 0;
+    if (c.weight_dtype == DEC_DTYPE_BF16 && R >= 2) {
+        const int qkv_n = (int)((Hq + 2 * Hkv) * hd);
+        for (size_t need : {gemv_tc_part_floats(R, (int)d, qkv_n, false), gemv_tc_part_floats(R, (int)(Hq * hd), (int)d, false),
+                            gemv_tc_part_floats(R, (int)d, (int)(2 * F), true), gemv_tc_part_floats(R, (int)F, (int)d, false),
+                            gemv_tc_part_floats(R, (int)d, (int)V, false)})
+            gp = need > gp ? need : gp;
+    }
+    L->gpart = take(gp * 4);
+    L->gcnt = take(gp ? GEMV_TC_CNT_WORDS * sizeof(unsigned) : 0);
+    // chained steps: counter, sticky error word, id and flag histories
+    L->chain = take(2 * sizeof(int) + 2 * (size_t)CHAIN_MAX * R * sizeof(int));
     L->rope = take((size_t)cap * (hd / 2) * sizeof(float2));
     const size_t es = (size_t)es_of(c.kv_dtype);
     if (layout == DEC_KV_PAGED)
@@ -130,6 +144,7 @@ struct dec_handle {
     int32_t* h_slots = nullptr;
     StatusBlock* h_status = nullptr;
     float* h_logits = nullptr;
+    int* h_chain = nullptr;        // pinned: [2 + 2 * CHAIN_MAX * rows] chain read-back
     std::vector<int32_t> slot_map_host;
 
     // recorded launches
@@ -296,6 +311,9 @@ cudaError_t zero_state(dec_handle* h) {
         return e;
     if ((e = cudaMemsetAsync(h->d_slots, 0, 3 * sizeof(int32_t) * h->rows, h->stream)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(h->d_counters, 0, sizeof(unsigned) * h->rows * h->cfg.n_kv_heads, h->stream)) != cudaSuccess)
+        return e;
+    if (h->lay.gcnt != h->lay.gpart &&
+        (e = cudaMemsetAsync(h->ws + h->lay.gcnt, 0, GEMV_TC_CNT_WORDS * sizeof(unsigned), h->stream)) != cudaSuccess)
         return e;
     return cudaMemsetAsync(h->d_x, 0, sizeof(float) * h->rows * h->cfg.d_model, h->stream);
 }
@@ -500,6 +518,9 @@ int dec_capture(dec_handle* h, int32_t cap, int32_t rows, int32_t kv_layout, int
         return cuda_fail(h, e, "cudaHostAlloc");
     if ((e = cudaHostAlloc((void**)&h->h_status, sizeof(StatusBlock), cudaHostAllocDefault)) != cudaSuccess)
         return cuda_fail(h, e, "cudaHostAlloc");
+    if ((e = cudaHostAlloc((void**)&h->h_chain, (2 + 2 * (size_t)CHAIN_MAX * rows) * sizeof(int),
+                           cudaHostAllocDefault)) != cudaSuccess)
+        return cuda_fail(h, e, "cudaHostAlloc");
     if ((e = cudaHostAlloc((void**)&h->h_logits, sizeof(float) * rows * (size_t)c.vocab, cudaHostAllocDefault)) !=
         cudaSuccess)
         return cuda_fail(h, e, "cudaHostAlloc");
@@ -555,6 +576,8 @@ int dec_capture(dec_handle* h, int32_t cap, int32_t rows, int32_t kv_layout, int
         p.nonfinite = h->d_status->nonfinite;
         p.err = &h->d_status->err;
         p.trace = h->d_trace;
+        p.tc_part = (float*)(h->ws + h->lay.gpart);
+        p.tc_cnt = (unsigned*)(h->ws + h->lay.gcnt);
         return pl;
     };
     for (int l = 0; l < c.n_layers; ++l) {
@@ -776,6 +799,78 @@ int dec_wait(dec_handle* h, float* logits_out, int32_t* ids_out, uint8_t* nonfin
     if (rc) return rc;
     if (h->state == ST_NEEDS_RESET) return fail(h, DEC_E_NEEDS_RESET, "an earlier step failed; call dec_reset_state");
     return finish_step(h, logits_out, ids_out, nonfinite_out);
+}
+
+int dec_chain(dec_handle* h, int32_t n_steps, const int32_t* tokens, const int32_t* pos, int32_t* ids_out,
+              uint8_t* nonfinite_out) {
+    const auto t0 = std::chrono::steady_clock::now();
+    int rc = gate(h, true);
+    if (rc) return rc;
+    if (h->state == ST_NEEDS_RESET) return fail(h, DEC_E_NEEDS_RESET, "an earlier step failed; call dec_reset_state");
+    if (!tokens || !pos || !ids_out) return fail(h, DEC_E_INVALID, "tokens, pos and ids_out are required");
+    if (n_steps < 1 || n_steps > CHAIN_MAX)
+        return fail(h, DEC_E_RANGE, "n_steps = %d outside [1, %d]", n_steps, CHAIN_MAX);
+    const int R = h->rows;
+    for (int r = 0; r < R; ++r) {
+        if (tokens[r] < 0 || tokens[r] >= h->cfg.vocab)
+            return fail(h, DEC_E_RANGE, "token[%d] = %d outside [0, %d)", r, tokens[r], h->cfg.vocab);
+        if (pos[r] < 0 || (int64_t)pos[r] + n_steps > h->cap)
+            return fail(h, DEC_E_RANGE, "pos[%d] = %d: a chain of %d steps leaves [0, %d)", r, pos[r], n_steps, h->cap);
+    }
+    for (int r = 0; r < R; ++r) {
+        h->h_slots[r] = tokens[r];
+        h->h_slots[R + r] = pos[r];
+        h->h_slots[2 * R + r] =
+            h->layout == DEC_KV_PAGED ? h->slot_map_host[(size_t)r * h->ppr + pos[r] / h->page] * h->page + pos[r] % h->page
+                                      : 0;
+    }
+    int* d_chain = (int*)(h->ws + h->lay.chain);
+    cudaError_t e = cudaMemcpyAsync(h->d_slots, h->h_slots, 3 * sizeof(int32_t) * R, cudaMemcpyHostToDevice, h->stream);
+    if (e != cudaSuccess) return cuda_fail(h, e, "slot write");
+    if ((e = cudaMemsetAsync(d_chain, 0, 2 * sizeof(int), h->stream)) != cudaSuccess) return cuda_fail(h, e, "chain clear");
+    ChainParams cp{};
+    cp.tok = h->d_slots;
+    cp.pos = h->d_slots + R;
+    cp.wm = h->d_slots + 2 * R;
+    cp.slot_map = h->layout == DEC_KV_PAGED ? h->d_slot_map : nullptr;
+    cp.R = R;
+    cp.V = h->cfg.vocab;
+    cp.cap = h->cap;
+    cp.ppr = h->ppr;
+    cp.page = h->page > 0 ? h->page : 1;
+    cp.amax = h->d_status->amax;
+    cp.nonfinite = h->d_status->nonfinite;
+    cp.err = &h->d_status->err;
+    cp.counter = d_chain;
+    cp.chain_err = reinterpret_cast<unsigned*>(d_chain + 1);
+    cp.ids = d_chain + 2;
+    cp.nf = d_chain + 2 + (size_t)CHAIN_MAX * R;
+    cp.max_steps = CHAIN_MAX;
+    for (int i = 0; i < n_steps; ++i) {
+        if ((rc = launch_step(h)) != DEC_OK) return rc;
+        if ((e = chain_advance_launch(cp, h->stream)) != cudaSuccess) return cuda_fail(h, e, "chain advance");
+    }
+    // one read-back: counter, sticky error, then the two histories
+    const size_t hist = (size_t)n_steps * R * sizeof(int);
+    if ((e = cudaMemcpyAsync(h->h_chain, d_chain, 2 * sizeof(int) + hist, cudaMemcpyDeviceToHost, h->stream)) !=
+            cudaSuccess ||
+        (e = cudaMemcpyAsync(h->h_chain + 2 + (size_t)CHAIN_MAX * R, cp.nf, hist, cudaMemcpyDeviceToHost, h->stream)) !=
+            cudaSuccess)
+        return cuda_fail(h, e, "chain readback");
+    if ((rc = bounded_wait(h)) != DEC_OK) return rc;
+    h->steps += n_steps;
+    const unsigned err = (unsigned)h->h_chain[1];
+    if (err || h->h_chain[0] != n_steps) {
+        h->last_fault = err;
+        h->state = ST_NEEDS_RESET;
+        return fail(h, DEC_E_DEVICE_FAULT, "device check failed in a chained step (error word 0x%x); results "
+                    "discarded, reset needed", err);
+    }
+    memcpy(ids_out, h->h_chain + 2, hist);
+    if (nonfinite_out)
+        for (size_t k = 0; k < (size_t)n_steps * R; ++k) nonfinite_out[k] = h->h_chain[2 + (size_t)CHAIN_MAX * R + k] ? 1 : 0;
+    h->last_step_us = std::chrono::duration<double, std::micro>(std::chrono::steady_clock::now() - t0).count() / n_steps;
+    return DEC_OK;
 }
 
 int dec_set_strategy(dec_handle* h, int32_t strategy) {
@@ -1046,6 +1141,7 @@ int dec_destroy(dec_handle* h) {
         if (h->h_slots) cudaFreeHost(h->h_slots);
         if (h->h_status) cudaFreeHost(h->h_status);
         if (h->h_logits) cudaFreeHost(h->h_logits);
+        if (h->h_chain) cudaFreeHost(h->h_chain);
         if (h->ev) cudaEventDestroy(h->ev);
         if (h->own_stream && h->stream) cudaStreamDestroy(h->stream);
     }

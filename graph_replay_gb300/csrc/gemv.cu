@@ -7,7 +7,7 @@ namespace gd {
 
 const void* gemv_kernel_bf16(int nr, int cpl, int pro, int epi);
 const void* gemv_kernel_f32(int nr, int cpl, int pro, int epi);
-const void* gemv_tc_kernel(int pro, int epi);
+const void* gemv_tc_kernel(int pro, int epi, int ws);
 cudaError_t gemv_tc_plan(GemvPlan* plan, int num_sms);
 
 namespace {
@@ -20,7 +20,7 @@ constexpr int MAX_S = 6;
 constexpr int MAX_RPS = 32;
 
 const void* pick(const GemvPlan& pl) {
-    if (pl.tc) return gemv_tc_kernel(pl.pro, pl.epi);
+    if (pl.tc) return gemv_tc_kernel(pl.pro, pl.epi, pl.p.tc_ws);
     return pl.wtype == W_BF16 ? gemv_kernel_bf16(pl.nr, pl.cpl, pl.pro, pl.epi)
                               : gemv_kernel_f32(pl.nr, pl.cpl, pl.pro, pl.epi);
 }

@@ -2,10 +2,10 @@
 //
 // With several decode rows every projection is a small dense contraction
 // out[r, n] = sum_k W[n, k] a[r, k] over r < R <= 8.  A CUDA-core GEMV would
-// have to keep R activation values per weight column on chip (R x K fp32:
-// 458 KB for the 8B-shape down projection at R = 8), so this kernel runs the
-// contraction on the tensor cores instead (mma.sync m16n8k16, bf16 in, fp32
-// accumulate) with the operands arranged so that nothing is wasted:
+// have to keep R activation values per weight column on chip in fp32 and
+// spend R FMAs per weight element; here the contraction runs on the tensor
+// cores (mma.sync m16n8k16, bf16 in, fp32 accumulate) with the operands
+// arranged so that no tensor-core row is wasted:
 //   A (16 x 16) = the activations: rows 0..7 are the bf16 "hi" parts of the
 //                 R decode rows, rows 8..15 the bf16 remainders a - hi ("lo"),
 //                 so the products keep ~16 significant bits of the fp32
@@ -18,21 +18,34 @@
 // it reads as whole 16-byte vectors (no ldmatrix, no swizzled layout).
 //
 // Data movement (one CTA per SM, balanced contiguous row ranges):
-//   * a stage is (up to 64 weight rows) x 256 columns plus the matching 256
-//     columns of the R activation rows; a producer warp fills a ring of stages
-//     with bulk asynchronous copies (cp.async.bulk, one 512-byte piece per
-//     weight row, mbarrier completion), and refills a slot once all eight
-//     compute warps have released it (one "empty" mbarrier per slot);
-//   * the weight copies of the first ring fill are issued before the
-//     programmatic-launch wait (weights do not depend on the previous kernel);
-//     the activation copies after it;
-//   * compute warp w takes the 64-column box (w & 3) of every stage for the
-//     tiles of parity (w >> 2); it builds its A fragments once per stage
-//     (RMSNorm scale and gain applied in registers) and reuses them for every
-//     tile;
-//   * the four boxes' partial tiles are added in fixed order in shared memory
-//     at the end of each row group, followed by the epilogue (store, residual
-//     add, logits + greedy argmax key, or SwiGLU of a gate/up pair).
+//   * each CTA owns one row range and one range of K (K is split over
+//     several CTAs only when the activations of the whole K do not fit in
+//     shared memory); its activation rows arrive with one bulk copy per row
+//     and stay resident; the compute warps convert them in place into bf16
+//     hi/lo pairs in fragment order (gain applied) and take the sum of
+//     squares in the same pass -- the RMSNorm scale 1/rms(x) is a per-row
+//     factor and is applied to the dot products in the epilogue;
+//   * the weights stream through a ring of stages of one 8-row tile x up to
+//     2048 columns: a producer warp issues one bulk asynchronous copy
+//     (cp.async.bulk, mbarrier completion) per weight row -- whole 2-4 KB row
+//     pieces keep the copy engine's per-copy cost small -- and refills a slot
+//     once the eight compute warps that took it have released it (one
+//     "empty" mbarrier per slot); the weights do not depend on the previous
+//     kernel, so the first stage is issued before the programmatic-launch
+//     wait, the activations right after it;
+//   * sixteen compute warps in two sets take alternate tiles; warp w of a set
+//     takes the 64-column boxes w, w+8, ... of its stages and accumulates its
+//     tiles of a row group (up to 8 tiles) in registers; at the end of the
+//     group the eight box warps' partial tiles are added in warp order in
+//     shared memory, followed by the epilogue (store, residual add, logits +
+//     greedy argmax key, or SwiGLU of a gate/up pair);
+//   * every shared-memory row (weight stage rows, activation rows) is padded
+//     by 64 bytes, so even and odd rows start 16 banks apart and a warp's
+//     16-byte fragment reads are conflict-free;
+//   * with K split over ks CTAs, each writes its partial sums (and its part of
+//     the sum of squares) to global scratch; the last of the ks CTAs to
+//     arrive at the row range's counter adds them in split order and applies
+//     the epilogue, then clears the counter for the next launch.
 // Results do not depend on scheduling: every sum has a fixed order.
 // Every mbarrier wait is bounded; a wait that gives up sets FAULT_WAIT in the
 // error word, the CTA stops consuming and issuing, and the producer waits
@@ -51,17 +64,19 @@
 namespace gd {
 
 namespace {
-constexpr int TC_WK = 256;                    // weight columns per stage
-constexpr int TC_ROWB = TC_WK * 2;            // bytes of one weight-row piece
-constexpr int TC_ACTB = TC_WK * 4;            // bytes of one activation-row piece
-constexpr int TC_ACT_SLOT = 8 * TC_ACTB;      // activation bytes per slot (8 rows reserved)
-constexpr int TC_CW = 8;                      // compute warps: 4 boxes x 2 tile parities
+constexpr int TC_BW = 8;                      // box warps: warp w takes boxes (w & 7) + 8i of a stage
+constexpr int TC_CW = 2 * TC_BW;              // compute warps: two sets take alternate tiles
 constexpr int TC_CT = TC_CW * 32;             // compute threads
 constexpr int TC_THREADS = TC_CT + 32;        // + the producer warp
-constexpr int TC_MAX_SR = 64;                 // weight rows per stage at most
-constexpr int TC_MAX_TW = TC_MAX_SR / 8 / 2;  // tiles per compute warp per stage at most
-constexpr int TC_MAX_S = 8;                   // ring stages at most
-constexpr int TC_RING_DEFAULT = 96 * 1024;    // ring bytes (leaves room for the next kernel's CTA)
+constexpr int TC_GT = 8;                      // tiles (8 weight rows each) per row group
+constexpr int TC_PAD = 64;                    // bytes after every shared-memory row: even and odd
+                                              // rows start 16 banks apart, so the fragment reads
+                                              // of a warp never collide
+constexpr int TC_MAX_S = 12;                  // ring stages at most
+constexpr int TC_WS_MAX = 2048;               // weight columns per stage at most
+constexpr int TC_WS_MIN = 1024;               // ... at least
+constexpr int TC_ACT_BUDGET_DEFAULT = 64 * 1024;    // shared memory for the resident activations (leaves
+                                                    // ~130 KB of ring; measured best of 32/64/128 KB)
 
 // source of weight row n (an index into the stacked segments) at column k0
 __device__ __forceinline__ const unsigned char* tc_row_src(const GemvParams& p, int n, int k0) {
@@ -74,48 +89,56 @@ __device__ __forceinline__ const unsigned char* tc_row_src(const GemvParams& p, 
     return reinterpret_cast<const unsigned char*>(w) + ((size_t)(n - base) * p.K + k0) * 2;
 }
 
-__device__ __forceinline__ float4 lds_f4(const void* p) { return *reinterpret_cast<const float4*>(p); }
 __device__ __forceinline__ uint4 lds_u4(const void* p) { return *reinterpret_cast<const uint4*>(p); }
-__device__ __forceinline__ float4 sel4(bool c, const float4& a, const float4& b) {
-    return make_float4(c ? a.x : b.x, c ? a.y : b.y, c ? a.z : b.z, c ? a.w : b.w);
-}
-__device__ __forceinline__ uint4 selu4(bool c, const uint4& a, const uint4& b) {
-    return make_uint4(c ? a.x : b.x, c ? a.y : b.y, c ? a.z : b.z, c ? a.w : b.w);
-}
+
+// acquire-ordered read of another CTA's partial sum (bypasses L1)
+__device__ __forceinline__ float ld_part(const float* p) { return __ldcg(p); }
 }  // namespace
 
 // EPI_SWIGLU (paired mode): segments 0 and 1 are the gate and up matrices with
 // the same row count F; out[r, n] = silu(gate_n . a_r) * (up_n . a_r), n < F.
-template <int PRO, int EPI>
-__global__ void __launch_bounds__(TC_THREADS, 2) k_gemv_tc(const GemvParams p) {
+template <int PRO, int EPI, int NBW>
+__global__ void __launch_bounds__(TC_THREADS, 1) k_gemv_tc(const GemvParams p) {
     constexpr bool PAIRED = EPI == EPI_SWIGLU;
+    constexpr bool RMS = PRO == PRO_RMSNORM;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ __align__(8) uint64_t full_bar[TC_MAX_S];
     __shared__ __align__(8) uint64_t empty_bar[TC_MAX_S];
-    __shared__ float nrm_s[TC_CW][8];
+    __shared__ __align__(8) uint64_t act_bar;
+    __shared__ float ss_s[TC_CW][8];
+    __shared__ float inv_s[8];
     __shared__ unsigned long long best_s[8];
     __shared__ unsigned nonfin_s;
-    __shared__ int abort_s;
+    __shared__ int abort_s, last_s;
     volatile int* abort_v = &abort_s;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int K = p.K, R = p.R, S = p.stages, GRW = p.rps;
-    const int SR = PAIRED ? 2 * GRW : GRW;              // weight rows of a full stage
-    const int NU = PAIRED ? p.seg_rows[0] : p.N;        // rows the CTAs divide
-    const int row0 = (int)(((long long)blockIdx.x * NU) / gridDim.x);
-    const int row1 = (int)(((long long)(blockIdx.x + 1) * NU) / gridDim.x);
-    const int NW = K / TC_WK;
+    constexpr int WS = NBW * 64 * TC_BW;                   // weight columns per stage
+    constexpr int WROW = WS * 2 + TC_PAD;                  // shared-memory pitch of a stage row
+    const int R = p.R, S = p.stages, KS = p.tc_ks;
+    const int TPG = PAIRED ? TC_GT / 2 : TC_GT;           // row tiles per group
+    const int GRW = TPG * 8;                               // rows per group
+    const int NU = PAIRED ? p.seg_rows[0] : p.N;          // rows the row ranges divide
+    const int q = blockIdx.x % KS, ri = blockIdx.x / KS, nrr = gridDim.x / KS;
+    const int KQ = p.K / KS, kq0 = q * KQ;                 // this CTA's K range
+    const int row0 = (int)(((long long)ri * NU) / nrr);
+    const int row1 = (int)(((long long)(ri + 1) * NU) / nrr);
     const int ngroups = (row1 - row0 + GRW - 1) / GRW;
-    const int nst = ngroups * NW;
-    const size_t slot_bytes = (size_t)SR * TC_ROWB + TC_ACT_SLOT;
+    const int nwin = KQ / WS;
+    const int nbx = KQ / 64;                               // 64-column boxes of the K range
+    const size_t slot_bytes = (size_t)8 * WROW;
+    const size_t arow = (size_t)KQ * 4 + TC_PAD;                            // pitch of an activation row
     unsigned char* ring = smem;
-    float* red = reinterpret_cast<float*>(smem + (size_t)S * slot_bytes);   // [4 boxes][SR][8]
+    unsigned char* act_s = smem + (size_t)S * slot_bytes;                   // [R][nbx][256 B] + pad per row
+    float* red = reinterpret_cast<float*>(act_s + (size_t)R * arow);       // [8 box warps][TC_GT * 8][8]
+    __nv_bfloat16* gain_s = reinterpret_cast<__nv_bfloat16*>(red + TC_BW * TC_GT * 8 * 8);   // [KQ] (RMSNorm)
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&full_bar[s], 1);
-            mbar_init(&empty_bar[s], TC_CW);
+            mbar_init(&empty_bar[s], TC_BW);   // the eight warps of the set that takes the stage
         }
+        mbar_init(&act_bar, 1);
         abort_s = 0;
         nonfin_s = 0u;
         mbar_fence_init();
@@ -125,69 +148,72 @@ __global__ void __launch_bounds__(TC_THREADS, 2) k_gemv_tc(const GemvParams p) {
 
     // ---------------- producer warp ----------------
     if (warp == TC_CW) {
-        auto stage_of = [&](int s, int& ga, int& nr, int& k0) {
-            ga = row0 + (s / NW) * GRW;
-            nr = min(GRW, row1 - ga);
-            k0 = (s % NW) * TC_WK;
-        };
-        auto expect = [&](int s) {
-            int ga, nr, k0;
-            stage_of(s, ga, nr, k0);
-            const uint32_t bytes = (uint32_t)((PAIRED ? 2 : 1) * nr * TC_ROWB + R * TC_ACTB);
-            if (lane == 0) mbar_arrive_expect_tx(&full_bar[s % S], bytes);
-            __syncwarp();
-        };
-        auto copy_w = [&](int s) {
-            int ga, nr, k0;
-            stage_of(s, ga, nr, k0);
-            unsigned char* dst = ring + (size_t)(s % S) * slot_bytes;
-            const int total = (PAIRED ? 2 : 1) * nr;
-            for (int i = lane; i < total; i += 32) {
-                const int half = (PAIRED && i >= nr) ? 1 : 0;
-                const int rr = i - half * nr;
-                const unsigned char* src =
-                    PAIRED ? reinterpret_cast<const unsigned char*>(p.w[half]) + ((size_t)(ga + rr) * K + k0) * 2
-                           : tc_row_src(p, ga + rr, k0);
-                bulk_g2s(dst + (size_t)(half * GRW + rr) * TC_ROWB, src, TC_ROWB, &full_bar[s % S]);
+        // stage s = (group, window, tile); the compute warps walk the same sequence
+        auto issue = [&](int s, int& issued) -> bool {
+                    int rem = s, gi = 0, ga = 0, nr = 0, nth = 0, ntl = 0;
+            for (gi = 0; gi < ngroups; ++gi) {
+                ga = row0 + gi * GRW;
+                nr = min(GRW, row1 - ga);
+                nth = (nr + 7) >> 3;
+                ntl = PAIRED ? 2 * nth : nth;
+                if (rem < nwin * ntl) break;
+                rem -= nwin * ntl;
             }
-        };
-        auto copy_a = [&](int s) {
-            int ga, nr, k0;
-            stage_of(s, ga, nr, k0);
-            unsigned char* dst = ring + (size_t)(s % S) * slot_bytes + (size_t)SR * TC_ROWB;
-            for (int r = lane; r < R; r += 32)
-                bulk_g2s(dst + r * TC_ACTB, p.act + (size_t)r * p.act_stride + k0, TC_ACTB, &full_bar[s % S]);
-        };
-        const int pre = min(S, nst);
-        for (int s = 0; s < pre; ++s) {
-            expect(s);
-            copy_w(s);
-        }
-        pdl_wait();   // the activations come from the previous kernel
-        for (int s = 0; s < pre; ++s) copy_a(s);
-        int issued = pre;
-        for (int s = pre; s < nst; ++s) {
+            const int w = rem / ntl, jj = rem % ntl;
+            const int half = (PAIRED && jj >= nth) ? 1 : 0;
+            const int ta = ga + 8 * (jj - half * nth);    // first row of the tile
+            const int tv = min(8, ga + nr - ta);           // valid rows of the tile
+            const int k0 = kq0 + w * WS;
             int ok = 1;
             if (lane == 0) {
                 if (*abort_v) {
                     ok = 0;
-                } else if (!mbar_wait(&empty_bar[s % S], ((s / S) - 1) & 1)) {
+                } else if (s >= S && !mbar_wait(&empty_bar[s % S], ((s / S) - 1) & 1)) {
                     ok = 0;
                     *abort_v = 1;
                     atomicOr(p.err, FAULT_WAIT);
+                } else {
+                    mbar_arrive_expect_tx(&full_bar[s % S], (uint32_t)(tv * WS * 2));
                 }
             }
-            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-            expect(s);
-            copy_w(s);
-            copy_a(s);
+            if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+            if (lane < tv) {
+                const unsigned char* src =
+                    PAIRED ? reinterpret_cast<const unsigned char*>(p.w[half]) + ((size_t)(ta + lane) * p.K + k0) * 2
+                           : tc_row_src(p, ta + lane, k0);
+                bulk_g2s(ring + (size_t)(s % S) * slot_bytes + (size_t)lane * WROW, src, (uint32_t)(WS * 2),
+                         &full_bar[s % S]);
+            }
             issued = s + 1;
+            return true;
+        };
+        int nst = 0;
+        for (int gi = 0; gi < ngroups; ++gi) {
+            const int nr = min(GRW, row1 - (row0 + gi * GRW));
+            nst += nwin * (PAIRED ? 2 : 1) * ((nr + 7) >> 3);
         }
+        int issued = 0;
+        bool go = true;
+        // the first weight stage, then the activations (they come from the
+        // previous kernel and gate every MMA), then the rest of the ring
+        if (nst > 0) go = issue(0, issued);
+        pdl_wait();
+        if (lane == 0)
+            mbar_arrive_expect_tx(&act_bar, (uint32_t)((size_t)R * KQ * 4 + (RMS ? (size_t)KQ * 2 : 0)));
+        __syncwarp();
+        if (lane < R)
+            bulk_g2s(act_s + (size_t)lane * arow, p.act + (size_t)lane * p.act_stride + kq0, (uint32_t)(KQ * 4),
+                     &act_bar);
+        if (RMS && lane == 31)
+            bulk_g2s(gain_s, reinterpret_cast<const __nv_bfloat16*>(p.gain) + kq0, (uint32_t)(KQ * 2), &act_bar);
+        for (int s = 1; s < nst && go; ++s) go = issue(s, issued);
         // no copy may still be landing when the CTA exits (only after an abort
         // can an issued stage be unconsumed)
-        if (lane == 0)
+        if (lane == 0) {
             for (int s = max(0, issued - S); s < issued; ++s)
                 if (!mbar_wait(&full_bar[s % S], (s / S) & 1)) atomicOr(p.err, FAULT_WAIT);
+            if (!mbar_wait(&act_bar, 0)) atomicOr(p.err, FAULT_WAIT);
+        }
         return;
     }
 
@@ -199,164 +225,206 @@ __global__ void __launch_bounds__(TC_THREADS, 2) k_gemv_tc(const GemvParams p) {
     }
     pdl_wait();
     if (tid == 0) trace_mark(tr, p.trace_id, 1);
-    const int g = lane >> 2, t = lane & 3;   // mma group (activation row / weight row of a tile), thread in group
-    const int box = warp & 3, par = warp >> 2;
-    const bool odd = (g & 1) != 0;           // odd rows take their two 16-byte halves in the other order
+    pdl_trigger();
+    const int g = lane >> 2, t = lane & 3;   // mma group (activation row / tile row), thread in group
+    const int bw = warp & (TC_BW - 1), par = warp / TC_BW;   // box warp, tile parity
 
-    float inv = 1.f;   // RMSNorm scale of activation row g
-    if (PRO == PRO_RMSNORM) {
+    // resident activations: box (r, b) holds 64 fp32 values as copied and is
+    // rewritten in place as four 64-byte quads [hi cols 8t.. | hi cols 32+8t.. |
+    // lo cols 8t.. | lo cols 32+8t..], each [t][8 x bf16]; lane l converts
+    // columns 2l, 2l+1 of the box (conflict-free 8-byte reads, 4-byte writes)
+    if (!*abort_v && !mbar_wait(&act_bar, 0)) {
+        *abort_v = 1;
+        atomicOr(p.err, FAULT_WAIT);
+    }
+    {
+        const int c = 2 * lane, ch = c >> 3, e = c & 7;
+        const int qoff = (ch >> 2) * 64 + (ch & 3) * 16 + e * 2;    // hi position; lo at +128
+        float ss[8];
 #pragma unroll
         for (int r = 0; r < 8; ++r) {
-            float ss = 0.f;
-            if (r < R) {
-                const float* a = p.act + (size_t)r * p.act_stride;
-                for (int k = tid * 4; k < K; k += TC_CT * 4) {
-                    const float4 x = *reinterpret_cast<const float4*>(a + k);
-                    ss = fmaf(x.x, x.x, ss);
-                    ss = fmaf(x.y, x.y, ss);
-                    ss = fmaf(x.z, x.z, ss);
-                    ss = fmaf(x.w, x.w, ss);
+            ss[r] = 0.f;
+            if (r < R) {   // warp-uniform (after a timeout the stale bytes are converted harmlessly)
+                for (int b = warp; b < nbx; b += TC_CW) {
+                    unsigned char* box = act_s + (size_t)r * arow + (size_t)b * 256;
+                    const float2 x = *reinterpret_cast<const float2*>(box + c * 4);
+                    ss[r] = fmaf(x.x, x.x, ss[r]);
+                    ss[r] = fmaf(x.y, x.y, ss[r]);
+                    float v0 = x.x, v1 = x.y;
+                    if (RMS) {
+                        const uint32_t gw = *reinterpret_cast<const uint32_t*>(gain_s + b * 64 + c);
+                        v0 *= bf16_lo(gw);
+                        v1 *= bf16_hi(gw);
+                    }
+                    const uint32_t hi = pack_bf16x2(v0, v1);
+                    const uint32_t lo = pack_bf16x2(v0 - bf16_lo(hi), v1 - bf16_hi(hi));
+                    __syncwarp();   // the whole box is read before it is rewritten
+                    *reinterpret_cast<uint32_t*>(box + qoff) = hi;
+                    *reinterpret_cast<uint32_t*>(box + 128 + qoff) = lo;
+                    __syncwarp();
                 }
             }
-            ss = warp_sum(ss);
-            if (lane == 0) nrm_s[warp][r] = ss;
+            ss[r] = warp_sum(ss[r]);
+        }
+        if (lane == 0) {
+#pragma unroll
+            for (int r = 0; r < 8; ++r) ss_s[warp][r] = ss[r];
         }
         named_sync(1, TC_CT);
-        if (g < R) {
+        if (tid < 8) {
             float tot = 0.f;
 #pragma unroll
-            for (int w = 0; w < TC_CW; ++w) tot += nrm_s[w][g];
-            inv = 1.0f / sqrtf(tot / (float)K + p.eps);
+            for (int w = 0; w < TC_CW; ++w) tot += ss_s[w][tid];
+            // the CTA's own sum of squares; with split K the last arriver adds the splits'
+            inv_s[tid] = RMS ? 1.0f / sqrtf(tot / (float)p.K + p.eps) : 1.f;
+            if (KS > 1 && RMS) p.tc_part[(size_t)KS * R * (PAIRED ? 2 * NU : NU) + ((size_t)q * nrr + ri) * 8 + tid] = tot;
         }
     }
-    pdl_trigger();
 
-    const __nv_bfloat16* gain = reinterpret_cast<const __nv_bfloat16*>(p.gain);
-    float acc[TC_MAX_TW][4];
+    float acc[TC_GT / 2][4];   // the tiles of this warp's parity
 #pragma unroll
-    for (int j = 0; j < TC_MAX_TW; ++j)
+    for (int j = 0; j < TC_GT / 2; ++j)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) acc[j][q] = 0.f;
+        for (int x = 0; x < 4; ++x) acc[j][x] = 0.f;
     unsigned long long best = 0ull;   // EPI_LOGITS: this thread's activation row is tid & 7
     bool nonfin = false;
+    // per-lane bases: activation row g (zero rows past R), stage row g, thread-in-group column offset
+    const unsigned char* abase = act_s + (size_t)(g < R ? g : 0) * arow + t * 16;
+    const size_t wofs = (size_t)g * WROW + t * 16;
+    const size_t np_stride = (size_t)(PAIRED ? 2 * NU : NU);   // partial sums per (split, activation row)
 
-    for (int s = 0; s < nst; ++s) {
-        const int slot = s % S;
-        const int grp = s / NW, win = s % NW;
-        const int ga = row0 + grp * GRW, nr = min(GRW, row1 - ga);
-        const int nt = (nr + 7) >> 3;                  // tiles per half
-        const int ntile = PAIRED ? 2 * nt : nt;
-        if (!*abort_v && !mbar_wait(&full_bar[slot], (s / S) & 1)) {
-            *abort_v = 1;
-            atomicOr(p.err, FAULT_WAIT);
+    // the epilogue of one output: v (and the up projection u when paired), unscaled
+    auto finish = [&](int r, int n, float v, float u, float iv) {
+        float* o = p.out + (size_t)r * p.out_stride + n;
+        v *= iv;
+        if (PAIRED) {
+            u *= iv;
+            *o = v / (1.0f + expf(-v)) * u;
+        } else if (EPI == EPI_ADD) {
+            *o += v;
+        } else {
+            *o = v;
         }
+        if (EPI == EPI_LOGITS) {
+            if (!isfinite(v)) nonfin = true;
+            const unsigned long long key = argmax_key(v, n);
+            best = key > best ? key : best;
+        }
+    };
+
+    int s = 0;
+    for (int gi = 0; gi < ngroups; ++gi) {
+        const int ga = row0 + gi * GRW, nr = min(GRW, row1 - ga);
+        const int nth = (nr + 7) >> 3;
+        const int ntl = PAIRED ? 2 * nth : nth;
+        for (int w = 0; w < nwin; ++w) {
+            const int bw0 = w * (WS / 64);   // first box of this window within the K range
+#pragma unroll
+            for (int jj = 0; jj < TC_GT; ++jj) {
+                if (jj < ntl) {
+                    const int slot = s % S;
+                    if ((jj & 1) == par) {
+                        if (!*abort_v && !mbar_wait(&full_bar[slot], (s / S) & 1)) {
+                            *abort_v = 1;
+                            atomicOr(p.err, FAULT_WAIT);
+                        }
+                        if (!*abort_v) {
+                            const unsigned char* st = ring + (size_t)slot * slot_bytes + wofs;
+#pragma unroll
+                            for (int i = 0; i < NBW; ++i) {
+                                const int bs = bw + TC_BW * i;   // box within the stage
+                                const unsigned char* ab = abase + (size_t)(bw0 + bs) * 256;
+                                uint4 q0 = lds_u4(ab), q1 = lds_u4(ab + 64), q2 = lds_u4(ab + 128), q3 = lds_u4(ab + 192);
+                                if (g >= R) q0 = q1 = q2 = q3 = make_uint4(0u, 0u, 0u, 0u);
+                                const uint4 w0 = lds_u4(st + bs * 128), w1 = lds_u4(st + bs * 128 + 64);
+                                // q0/q1: hi of columns 8t.. / 32+8t..; q2/q3: lo of the same
+                                const uint32_t a0[4] = {q0.x, q2.x, q0.y, q2.y};
+                                const uint32_t a1[4] = {q0.z, q2.z, q0.w, q2.w};
+                                const uint32_t a2[4] = {q1.x, q3.x, q1.y, q3.y};
+                                const uint32_t a3[4] = {q1.z, q3.z, q1.w, q3.w};
+                                mma_bf16(acc[jj >> 1], a0, w0.x, w0.y);
+                                mma_bf16(acc[jj >> 1], a1, w0.z, w0.w);
+                                mma_bf16(acc[jj >> 1], a2, w1.x, w1.y);
+                                mma_bf16(acc[jj >> 1], a3, w1.z, w1.w);
+                            }
+                        }
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&empty_bar[slot]);   // this warp is done with the slot
+                    }
+                    ++s;
+                }
+            }
+        }
+
+        // row group done: the eight warps' partial tiles, added in warp order
         const bool live = !*abort_v;
-        const unsigned char* st = ring + (size_t)slot * slot_bytes;
         if (live) {
-            // A fragments of this warp's box: activation row g, chunks t and 4+t
-            // (columns 8t..8t+7 and 32+8t..32+8t+7 of the box)
-            float4 q0 = make_float4(0.f, 0.f, 0.f, 0.f), q1 = q0, q2 = q0, q3 = q0;
-            if (g < R) {
-                const unsigned char* ar = st + (size_t)SR * TC_ROWB + g * TC_ACTB + box * 256 + t * 32;
-                // even rows: (t, lo half), (t, hi half), (4+t, lo), (4+t, hi); odd rows the reverse
-                const float4 v0 = lds_f4(ar + (odd ? 144 : 0));
-                const float4 v1 = lds_f4(ar + (odd ? 128 : 16));
-                const float4 v2 = lds_f4(ar + (odd ? 16 : 128));
-                const float4 v3 = lds_f4(ar + (odd ? 0 : 144));
-                q0 = sel4(odd, v3, v0);
-                q1 = sel4(odd, v2, v1);
-                q2 = sel4(odd, v1, v2);
-                q3 = sel4(odd, v0, v3);
-                if (PRO == PRO_RMSNORM) {
-                    const int kb = win * TC_WK + box * 64 + t * 8;
-                    float gl[8], gh[8];
-                    Elem<__nv_bfloat16>::unpack(__ldg(reinterpret_cast<const uint4*>(gain + kb)), gl);
-                    Elem<__nv_bfloat16>::unpack(__ldg(reinterpret_cast<const uint4*>(gain + kb + 32)), gh);
-                    q0 = make_float4(q0.x * inv * gl[0], q0.y * inv * gl[1], q0.z * inv * gl[2], q0.w * inv * gl[3]);
-                    q1 = make_float4(q1.x * inv * gl[4], q1.y * inv * gl[5], q1.z * inv * gl[6], q1.w * inv * gl[7]);
-                    q2 = make_float4(q2.x * inv * gh[0], q2.y * inv * gh[1], q2.z * inv * gh[2], q2.w * inv * gh[3]);
-                    q3 = make_float4(q3.x * inv * gh[4], q3.y * inv * gh[5], q3.z * inv * gh[6], q3.w * inv * gh[7]);
-                }
-            }
-            // k-step ks uses 4 consecutive values: ks 0 -> q0, 1 -> q1, 2 -> q2, 3 -> q3
-            uint32_t a[4][4];
-            auto frag = [&](const float4& v, uint32_t (&f)[4]) {
-                const uint32_t h01 = pack_bf16x2(v.x, v.y), h23 = pack_bf16x2(v.z, v.w);
-                f[0] = h01;
-                f[2] = h23;
-                f[1] = pack_bf16x2(v.x - bf16_lo(h01), v.y - bf16_hi(h01));
-                f[3] = pack_bf16x2(v.z - bf16_lo(h23), v.w - bf16_hi(h23));
-            };
-            frag(q0, a[0]);
-            frag(q1, a[1]);
-            frag(q2, a[2]);
-            frag(q3, a[3]);
 #pragma unroll
-            for (int jj = 0; jj < TC_MAX_TW; ++jj) {
-                const int j = par + 2 * jj;
-                if (j < ntile) {
-                    const int srow = (PAIRED && j >= nt) ? GRW + 8 * (j - nt) + g : 8 * j + g;
-                    const unsigned char* wr = st + (size_t)srow * TC_ROWB + box * 128 + t * 16;
-                    const uint4 u0 = lds_u4(wr + (odd ? 64 : 0));
-                    const uint4 u1 = lds_u4(wr + (odd ? 0 : 64));
-                    const uint4 w0 = selu4(odd, u1, u0), w1 = selu4(odd, u0, u1);   // chunk t, chunk 4+t
-                    mma_bf16(acc[jj], a[0], w0.x, w0.y);
-                    mma_bf16(acc[jj], a[1], w0.z, w0.w);
-                    mma_bf16(acc[jj], a[2], w1.x, w1.y);
-                    mma_bf16(acc[jj], a[3], w1.z, w1.w);
+            for (int j2 = 0; j2 < TC_GT / 2; ++j2) {
+                const int jj = 2 * j2 + par;
+                if (jj < ntl) {
+                    const int n0 = 8 * jj + 2 * t;
+                    red[((size_t)bw * TC_GT * 8 + n0) * 8 + g] = acc[j2][0] + acc[j2][2];
+                    red[((size_t)bw * TC_GT * 8 + n0 + 1) * 8 + g] = acc[j2][1] + acc[j2][3];
                 }
             }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty_bar[slot]);   // this warp is done with the slot
+#pragma unroll
+        for (int j2 = 0; j2 < TC_GT / 2; ++j2)
+#pragma unroll
+            for (int x = 0; x < 4; ++x) acc[j2][x] = 0.f;
+        named_sync(1, TC_CT);
+        if (live) {
+            const int r = tid & 7;
+            for (int idx = tid; idx < nr * 8; idx += TC_CT) {
+                const int n = idx >> 3;
+                if (r >= R) continue;
+                float v = 0.f, u = 0.f;
+#pragma unroll
+                for (int w = 0; w < TC_BW; ++w) v += red[((size_t)w * TC_GT * 8 + n) * 8 + r];
+                if (PAIRED) {
+#pragma unroll
+                    for (int w = 0; w < TC_BW; ++w) u += red[((size_t)w * TC_GT * 8 + 8 * nth + n) * 8 + r];
+                }
+                if (KS == 1) {
+                    finish(r, ga + n, v, u, inv_s[r]);
+                } else {
+                    float* pp = p.tc_part + ((size_t)q * R + r) * np_stride;
+                    pp[ga + n] = v;
+                    if (PAIRED) pp[NU + ga + n] = u;
+                }
+            }
+        }
+        named_sync(1, TC_CT);   // `red` is rewritten by the next group
+    }
 
-        if (win == NW - 1) {
-            // row group done: the four boxes' partial tiles, added in box order
-            if (live) {
-#pragma unroll
-                for (int jj = 0; jj < TC_MAX_TW; ++jj) {
-                    const int j = par + 2 * jj;
-                    if (j < ntile) {
-                        const int n0 = ((PAIRED && j >= nt) ? GRW + 8 * (j - nt) : 8 * j) + 2 * t;
-                        red[((size_t)box * SR + n0) * 8 + g] = acc[jj][0] + acc[jj][2];
-                        red[((size_t)box * SR + n0 + 1) * 8 + g] = acc[jj][1] + acc[jj][3];
-                    }
-                }
+    // split K: the last CTA of the row range adds the splits in order
+    if (KS > 1) {
+        __threadfence();
+        named_sync(1, TC_CT);
+        if (tid == 0) last_s = atomicAdd(p.tc_cnt + ri, 1u) == (unsigned)(KS - 1) ? 1 : 0;
+        named_sync(1, TC_CT);
+        if (last_s && !*abort_v) {
+            __threadfence();
+            if (tid < 8) {
+                float tot = 0.f;
+                for (int x = 0; x < KS; ++x) tot += ld_part(p.tc_part + (size_t)KS * R * np_stride + ((size_t)x * nrr + ri) * 8 + tid);
+                inv_s[tid] = RMS ? 1.0f / sqrtf(tot / (float)p.K + p.eps) : 1.f;
             }
-#pragma unroll
-            for (int jj = 0; jj < TC_MAX_TW; ++jj)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) acc[jj][q] = 0.f;
             named_sync(1, TC_CT);
-            if (live) {
-                const int r = tid & 7;
-                for (int idx = tid; idx < nr * 8; idx += TC_CT) {
-                    const int n = idx >> 3;
-                    if (r >= R) continue;
-                    float v = red[((size_t)0 * SR + n) * 8 + r];
-                    v += red[((size_t)1 * SR + n) * 8 + r];
-                    v += red[((size_t)2 * SR + n) * 8 + r];
-                    v += red[((size_t)3 * SR + n) * 8 + r];
-                    float* o = p.out + (size_t)r * p.out_stride + ga + n;
-                    if (PAIRED) {
-                        float u = red[((size_t)0 * SR + GRW + n) * 8 + r];
-                        u += red[((size_t)1 * SR + GRW + n) * 8 + r];
-                        u += red[((size_t)2 * SR + GRW + n) * 8 + r];
-                        u += red[((size_t)3 * SR + GRW + n) * 8 + r];
-                        *o = v / (1.0f + expf(-v)) * u;
-                    } else if (EPI == EPI_ADD) {
-                        *o += v;
-                    } else {
-                        *o = v;
-                    }
-                    if (EPI == EPI_LOGITS) {
-                        if (!isfinite(v)) nonfin = true;
-                        const unsigned long long key = argmax_key(v, ga + n);
-                        best = key > best ? key : best;
-                    }
+            const int r = tid & 7;
+            for (int idx = tid; idx < (row1 - row0) * 8; idx += TC_CT) {
+                const int n = row0 + (idx >> 3);
+                if (r >= R) continue;
+                float v = 0.f, u = 0.f;
+                for (int x = 0; x < KS; ++x) {
+                    const float* pp = p.tc_part + ((size_t)x * R + r) * np_stride;
+                    v += ld_part(pp + n);
+                    if (PAIRED) u += ld_part(pp + NU + n);
                 }
+                finish(r, n, v, u, inv_s[r]);
             }
-            named_sync(1, TC_CT);   // `red` is rewritten by the next group
+            if (tid == 0) p.tc_cnt[ri] = 0u;   // ready for the next launch
         }
     }
 
@@ -380,59 +448,106 @@ __global__ void __launch_bounds__(TC_THREADS, 2) k_gemv_tc(const GemvParams p) {
 
 // ---------------- host side ----------------
 
-const void* gemv_tc_kernel(int pro, int epi) {
-    if (pro == PRO_RMSNORM && epi == EPI_STORE) return (const void*)&k_gemv_tc<PRO_RMSNORM, EPI_STORE>;
-    if (pro == PRO_RMSNORM && epi == EPI_LOGITS) return (const void*)&k_gemv_tc<PRO_RMSNORM, EPI_LOGITS>;
-    if (pro == PRO_RMSNORM && epi == EPI_SWIGLU) return (const void*)&k_gemv_tc<PRO_RMSNORM, EPI_SWIGLU>;
-    if (pro == PRO_PLAIN && epi == EPI_ADD) return (const void*)&k_gemv_tc<PRO_PLAIN, EPI_ADD>;
-    if (pro == PRO_PLAIN && epi == EPI_STORE) return (const void*)&k_gemv_tc<PRO_PLAIN, EPI_STORE>;
+template <int NBW>
+const void* gemv_tc_pick(int pro, int epi) {
+    if (pro == PRO_RMSNORM && epi == EPI_STORE) return (const void*)&k_gemv_tc<PRO_RMSNORM, EPI_STORE, NBW>;
+    if (pro == PRO_RMSNORM && epi == EPI_LOGITS) return (const void*)&k_gemv_tc<PRO_RMSNORM, EPI_LOGITS, NBW>;
+    if (pro == PRO_RMSNORM && epi == EPI_SWIGLU) return (const void*)&k_gemv_tc<PRO_RMSNORM, EPI_SWIGLU, NBW>;
+    if (pro == PRO_PLAIN && epi == EPI_ADD) return (const void*)&k_gemv_tc<PRO_PLAIN, EPI_ADD, NBW>;
+    if (pro == PRO_PLAIN && epi == EPI_STORE) return (const void*)&k_gemv_tc<PRO_PLAIN, EPI_STORE, NBW>;
     return nullptr;
+}
+
+// the kernel for a plan: stage width 1024 (2 boxes per warp) or 2048 (4)
+const void* gemv_tc_kernel(int pro, int epi, int ws) {
+    return ws == 2048 ? gemv_tc_pick<4>(pro, epi) : ws == 1024 ? gemv_tc_pick<2>(pro, epi) : nullptr;
+}
+
+namespace {
+int act_budget() {
+    if (const char* env = getenv("GRAPHDEC_TC_ACT_KB")) {   // resident activation budget (tuning)
+        const long v = atol(env);
+        if (v >= 32 && v <= 160) return (int)v * 1024;
+    }
+    return TC_ACT_BUDGET_DEFAULT;
+}
+// K splits: the fewest whose K range is a multiple of the stage width
+// (>= 1024 columns) and whose activations fit the budget; 0 if none
+int tc_splits(int R, int K, int budget) {
+    for (int ks = 1; ks <= 64; ++ks) {
+        if (K % ks) continue;
+        const int kq = K / ks;
+        if (kq % TC_WS_MIN) continue;
+        if ((size_t)R * kq * 4 <= (size_t)budget) return ks;
+    }
+    return 0;
+}
+}  // namespace
+
+size_t gemv_tc_part_floats(int R, int K, int N, bool paired) {
+    // the largest need over the budgets the plan may use
+    size_t most = 0;
+    for (int budget : {32 * 1024, 64 * 1024, 96 * 1024, 128 * 1024, 160 * 1024, act_budget()}) {
+        const int ks = tc_splits(R, K, budget);
+        if (ks > 1) {
+            const size_t need = (size_t)ks * R * (size_t)N + (size_t)ks * GEMV_TC_CNT_WORDS * 8;
+            if (need > most) most = need;
+        }
+    }
+    (void)paired;   // N already counts both halves of a gate/up pair
+    return most;
 }
 
 cudaError_t gemv_tc_plan(GemvPlan* plan, int num_sms) {
     GemvParams& p = plan->p;
     const bool paired = plan->epi == EPI_SWIGLU;
     if (plan->wtype != W_BF16) return cudaErrorInvalidValue;
-    if (p.R < 1 || p.R > 8 || p.K <= 0 || p.K % TC_WK != 0 || p.N <= 0) return cudaErrorInvalidValue;
+    if (p.R < 1 || p.R > 8 || p.K <= 0 || p.K % TC_WS_MIN != 0 || p.N <= 0) return cudaErrorInvalidValue;
     if (paired && (p.seg_rows[0] != p.seg_rows[1] || p.seg_rows[2] != 0)) return cudaErrorInvalidValue;
-    // 16-byte aligned sources for every bulk copy: weight rows (K % 256 == 0),
-    // activation rows, and the segment bases
+    // 16-byte aligned sources: weight rows (K % 1024 == 0), activation rows, gains, segment bases
     if (p.act_stride % 4 != 0 || (reinterpret_cast<uintptr_t>(p.act) & 15u) != 0) return cudaErrorInvalidValue;
     for (int i = 0; i < 3; ++i)
         if (p.seg_rows[i] > 0 && (reinterpret_cast<uintptr_t>(p.w[i]) & 15u) != 0) return cudaErrorInvalidValue;
-    if (p.gain && (reinterpret_cast<uintptr_t>(p.gain) & 15u) != 0) return cudaErrorInvalidValue;
-    const void* fn = gemv_tc_kernel(plan->pro, plan->epi);
+    if (plan->pro == PRO_RMSNORM && (!p.gain || (reinterpret_cast<uintptr_t>(p.gain) & 15u) != 0))
+        return cudaErrorInvalidValue;
+    const void* fn = gemv_tc_kernel(plan->pro, plan->epi, TC_WS_MAX);
     if (!fn) return cudaErrorInvalidValue;
-    const int nu = paired ? p.seg_rows[0] : p.N;
-    const int grid = nu < num_sms ? nu : num_sms;
-    const int per_cta = (nu + grid - 1) / grid;
-    const int max_grw = paired ? TC_MAX_SR / 2 : TC_MAX_SR;
-    int grw = (per_cta + 7) / 8 * 8;
-    if (grw > max_grw) grw = max_grw;
-    const int sr = paired ? 2 * grw : grw;
-    const size_t slot = (size_t)sr * TC_ROWB + TC_ACT_SLOT;
-    size_t ring = TC_RING_DEFAULT;
-    if (const char* env = getenv("GRAPHDEC_TC_RING")) {   // ring bytes per CTA (tuning)
-        const long v = atol(env);
-        if (v >= 32768 && v <= 220 * 1024) ring = (size_t)v;
-    }
-    int S = (int)(ring / slot);
-    if (S > TC_MAX_S) S = TC_MAX_S;
-    if (S < 2) S = 2;
-    const size_t red = (size_t)4 * sr * 8 * sizeof(float);
+    const int ks = tc_splits(p.R, p.K, act_budget());
+    if (ks < 1) return cudaErrorInvalidValue;
+    const int kq = p.K / ks;
     int dev = 0, optin = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess) return e;
     cudaFuncAttributes fa;
     if ((e = cudaFuncGetAttributes(&fa, fn)) != cudaSuccess) return e;
-    while (S > 2 && (size_t)S * slot + red > (size_t)optin - fa.sharedSizeBytes) --S;
-    if ((size_t)S * slot + red > (size_t)optin - fa.sharedSizeBytes) return cudaErrorInvalidValue;
-    p.rps = grw;
+    const size_t avail = (size_t)optin - fa.sharedSizeBytes;
+    const size_t fixed = (size_t)p.R * ((size_t)kq * 4 + TC_PAD) + (size_t)TC_BW * TC_GT * 8 * 8 * sizeof(float) +
+                         (plan->pro == PRO_RMSNORM ? (size_t)kq * 2 : 0);
+    if (fixed >= avail) return cudaErrorInvalidValue;
+    // stage width: 2048 columns when at least 3 such stages fit, else 1024
+    int ws = (kq % TC_WS_MAX == 0) ? TC_WS_MAX : TC_WS_MIN;
+    auto slot_of = [](int w) { return (size_t)8 * ((size_t)w * 2 + TC_PAD); };
+    int S = (int)((avail - fixed) / slot_of(ws));
+    if (S < 3 && ws > TC_WS_MIN) {
+        ws = TC_WS_MIN;
+        S = (int)((avail - fixed) / slot_of(ws));
+    }
+    if (S > TC_MAX_S) S = TC_MAX_S;
+    if (S < 2) return cudaErrorInvalidValue;
+    const int nu = paired ? p.seg_rows[0] : p.N;
+    int nrr = num_sms / ks;                      // row ranges
+    if (nrr > nu) nrr = nu;
+    if (nrr < 1 || (ks > 1 && nrr > (int)GEMV_TC_CNT_WORDS)) return cudaErrorInvalidValue;
+    if (ks > 1 && (!p.tc_part || !p.tc_cnt)) return cudaErrorInvalidValue;
+    fn = gemv_tc_kernel(plan->pro, plan->epi, ws);   // same static shared memory at either width
+    p.rps = TC_GT;
     p.stages = S;
-    plan->grid = grid;
+    p.tc_ws = ws;
+    p.tc_ks = ks;
+    plan->grid = nrr * ks;
     plan->block = TC_THREADS;
-    plan->smem = (size_t)S * slot + red;
+    plan->smem = (size_t)S * slot_of(ws) + fixed;
     plan->nr = 8;
     plan->cpl = 0;
     return raise_smem_cap(fn);

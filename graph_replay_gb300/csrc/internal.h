@@ -51,8 +51,12 @@ struct GemvParams {
     unsigned long long* amax;  // [R] argmax keys (EPI_LOGITS)
     unsigned* nonfinite;       // [R] flags (EPI_LOGITS)
     unsigned* err;             // error word (FAULT_WAIT)
-    int rps;                   // weight rows per ring stage
+    int rps;                   // weight rows per ring stage (tensor-core GEMV: tiles per row group)
     int stages;                // ring stages
+    int tc_ws;                 // tensor-core GEMV: weight columns per stage
+    int tc_ks;                 // tensor-core GEMV: K splits (CTAs per row range)
+    float* tc_part;            // tensor-core GEMV, tc_ks > 1: partial sums [ks][R][N or 2F] + [ks][ranges][8] sums of squares
+    unsigned* tc_cnt;          // tensor-core GEMV, tc_ks > 1: arrivals per row range (zero between launches)
     unsigned long long* trace; // trace buffer or null
     int trace_id;
 };
@@ -67,6 +71,10 @@ struct GemvPlan {
 
 // Fill plan->grid/block/smem/nr/cpl and p.rps/p.stages for the given shape.
 cudaError_t gemv_plan(GemvPlan* plan, int num_sms);
+// Scratch of the tensor-core GEMV for rows x (K -> N) (paired: N = 2F): floats
+// of split partials, and the arrival counters (words), for any device.
+size_t gemv_tc_part_floats(int R, int K, int N, bool paired);
+constexpr size_t GEMV_TC_CNT_WORDS = 1024;
 cudaError_t gemv_launch(const GemvPlan& plan, cudaStream_t s, bool pdl);
 
 // ---------------- split-KV masked decode attention ----------------
@@ -129,6 +137,24 @@ struct EmbedParams {
     int trace_id;
 };
 cudaError_t embed_launch(int wtype, const EmbedParams& p, cudaStream_t s);
+
+// ---------------- chained greedy steps ----------------
+struct ChainParams {
+    int* tok;                        // [R] Token slot
+    int* pos;                        // [R] Pos slot
+    int* wm;                         // [R] WriteMap slot (paged)
+    const int* slot_map;             // [R, ppr] SlotMap (paged) or null
+    int R, V, cap, ppr, page;
+    const unsigned long long* amax;  // [R] greedy keys of the step just run
+    const unsigned* nonfinite;       // [R]
+    unsigned* err;                   // the step's error word
+    unsigned* chain_err;             // sticky over the chain
+    int* counter;                    // steps recorded so far
+    int* ids;                        // [max_steps, R] history
+    int* nf;                         // [max_steps, R] history
+    int max_steps;
+};
+cudaError_t chain_advance_launch(const ChainParams& p, cudaStream_t s);
 
 // a kernel that spins for about `ns` nanoseconds on one SM, then returns
 cudaError_t busy_launch(long long ns, cudaStream_t s);
