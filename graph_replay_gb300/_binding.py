@@ -75,6 +75,7 @@ _SIG = [
     ("dec_step", ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P]),
     ("dec_launch", ctypes.c_int, [_P, _P]),
     ("dec_wait", ctypes.c_int, [_P, _P, _P, _P]),
+    ("dec_chain", ctypes.c_int, [_P, _I32, _P, _P, _P, _P]),
     ("dec_set_strategy", ctypes.c_int, [_P, _I32]),
     ("dec_set_eager", ctypes.c_int, [_P, _I32]),
     ("dec_reset_state", ctypes.c_int, [_P]),
@@ -185,6 +186,13 @@ def dec_launch(h, dev_slots_ptr) -> int:
 
 def dec_wait(h, logits_ptr, ids_ptr, nonfinite_ptr) -> int:
     return lib().dec_wait(h, logits_ptr, ids_ptr, nonfinite_ptr)
+
+
+def dec_chain(h, n_steps: int, tokens_ptr, pos_ptr, ids_ptr, nonfinite_ptr) -> int:
+    return lib().dec_chain(h, n_steps, tokens_ptr, pos_ptr, ids_ptr, nonfinite_ptr)
+
+
+DEC_CHAIN_MAX_STEPS = 4096
 
 
 def dec_set_strategy(h, strategy: int) -> None:

@@ -64,6 +64,47 @@ cudaError_t embed_launch(int wtype, const EmbedParams& p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// Between two steps of a chain ("Models, Registry and the Driver", section
+// "The Driver": RowWork::Chain -- with no guided row, the device feeds each
+// pick to the next step and the host waits once).  One CTA of 32 threads,
+// thread r < R for row r:
+//   * keeps the step's error word in the chain's sticky word (the next step's
+//     first kernel clears the error word);
+//   * decodes the greedy key into the token id, records it and the non-finite
+//     flag in the history at the chain's step counter;
+//   * writes the slots of the next step: Token = the id, Pos += 1, and for
+//     paged KV the WriteMap slot of the new position from the SlotMap (only
+//     while Pos < cap; the host checks the chain stays below cap).
+__global__ void __launch_bounds__(32) k_chain_advance(const ChainParams p) {
+    const int r = threadIdx.x;
+    const int i = *p.counter;
+    if (r == 0) {
+        const unsigned e = *p.err;
+        if (e) atomicOr(p.chain_err, e);
+    }
+    if (r < p.R && i < p.max_steps) {
+        const unsigned long long k = p.amax[r];
+        int id = k ? (int)(0xFFFFFFFFu - (unsigned)(k & 0xFFFFFFFFull)) : -1;
+        if (id < 0 || id >= p.V) {
+            atomicOr(p.chain_err, FAULT_TOKEN);
+            id = 0;
+        }
+        p.ids[(size_t)i * p.R + r] = id;
+        p.nf[(size_t)i * p.R + r] = p.nonfinite[r] ? 1 : 0;
+        p.tok[r] = id;
+        const int np = p.pos[r] + 1;
+        p.pos[r] = np;
+        if (p.slot_map && np < p.cap) p.wm[r] = p.slot_map[(size_t)r * p.ppr + np / p.page] * p.page + np % p.page;
+    }
+    __syncwarp();
+    if (r == 0) *p.counter = i + 1;
+}
+
+cudaError_t chain_advance_launch(const ChainParams& p, cudaStream_t s) {
+    k_chain_advance<<<1, 32, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
 // Spins on the global nanosecond timer for `ns`, with an iteration cap as a
 // second bound, then returns: a kernel that is slow on purpose but always ends.
 __global__ void k_busy(long long ns) {

@@ -119,6 +119,17 @@ class Decoder:
         B.check(self.h, rc)
         return StepResult(self._logits.copy() if logits else None, self._ids.copy(), self._nf.copy())
 
+    def chain(self, tokens, pos, n_steps: int):
+        """n_steps chained greedy steps from (tokens, pos): the device feeds each
+        step's ids to the next; returns (ids [n_steps, rows], nonfinite [n_steps, rows])."""
+        tok = np.ascontiguousarray(tokens, dtype=np.int32).reshape(self.rows)
+        ps = np.ascontiguousarray(pos, dtype=np.int32).reshape(self.rows)
+        ids = np.empty((n_steps, self.rows), dtype=np.int32)
+        nf = np.empty((n_steps, self.rows), dtype=np.uint8)
+        self._after_torch()
+        B.check(self.h, B.dec_chain(self.h, int(n_steps), _ptr(tok), _ptr(ps), _ptr(ids), _ptr(nf)))
+        return ids, nf
+
     def launch(self, dev_slots: Optional[torch.Tensor]) -> None:
         """Asynchronous step from a device slot record [3*rows] int32 (tokens, pos, write map)."""
         self._after_torch()

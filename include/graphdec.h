@@ -232,6 +232,27 @@ int dec_launch(dec_handle *h, const int32_t *dev_slots);
  * the last step's error word is non-zero. */
 int dec_wait(dec_handle *h, float *logits_out, int32_t *ids_out, uint8_t *nonfinite_out);
 
+/* Chained greedy steps ("Models, Registry and the Driver", section "The
+ * Driver": RowWork::Chain -- with no guided row, several decode steps run back
+ * to back, the device feeds each step's pick to the next and the host waits
+ * once).  Step 0 runs tokens at pos; step i > 0 runs, for every row, the
+ * greedy id of step i - 1 at pos + i.  Each step is one replay of the recorded
+ * step followed by a one-CTA kernel that records the ids and writes the next
+ * step's Token, Pos and (paged) WriteMap slots from the device; the host
+ * copies the histories back once and waits once.
+ *   n_steps       1 .. DEC_CHAIN_MAX_STEPS
+ *   tokens, pos   host [rows], as for dec_step; pos[r] + n_steps <= cap
+ *                 (DEC_E_RANGE otherwise, before anything is launched)
+ *   ids_out       host [n_steps, rows]: the greedy id of each step (required)
+ *   nonfinite_out host [n_steps, rows] non-finite flags, or NULL
+ * Paged KV takes every WriteMap from the current slot map.  A device check
+ * that fails in any step of the chain returns DEC_E_DEVICE_FAULT (results
+ * discarded, reset needed).  The logits of the last step stay on the device
+ * (dec_logits_ptr). */
+#define DEC_CHAIN_MAX_STEPS 4096
+int dec_chain(dec_handle *h, int32_t n_steps, const int32_t *tokens, const int32_t *pos, int32_t *ids_out,
+              uint8_t *nonfinite_out);
+
 /* Choose the execution strategy (dec_strategy) for the coming dec_capture;
  * DEC_E_STATE after capture.  Default DEC_STRATEGY_GRAPH. */
 int dec_set_strategy(dec_handle *h, int32_t strategy);
