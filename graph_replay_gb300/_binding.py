@@ -76,6 +76,7 @@ _SIG = [
     ("dec_launch", ctypes.c_int, [_P, _P]),
     ("dec_wait", ctypes.c_int, [_P, _P, _P, _P]),
     ("dec_chain", ctypes.c_int, [_P, _I32, _P, _P, _P, _P]),
+    ("dec_prefill", ctypes.c_int, [_P, _P, _P, _I32, _I32, _P, _P]),
     ("dec_set_strategy", ctypes.c_int, [_P, _I32]),
     ("dec_set_eager", ctypes.c_int, [_P, _I32]),
     ("dec_reset_state", ctypes.c_int, [_P]),
@@ -193,6 +194,10 @@ def dec_chain(h, n_steps: int, tokens_ptr, pos_ptr, ids_ptr, nonfinite_ptr) -> i
 
 
 DEC_CHAIN_MAX_STEPS = 4096
+
+
+def dec_prefill(h, pages_ptr, tokens_ptr, n: int, pos0: int, logits_ptr, id_ptr) -> int:
+    return lib().dec_prefill(h, pages_ptr, tokens_ptr, n, pos0, logits_ptr, id_ptr)
 
 
 def dec_set_strategy(h, strategy: int) -> None:

@@ -126,14 +126,20 @@ __global__ void __launch_bounds__(AM_THREADS, 2) k_attn_mma(const __grid_constan
         for (int i = 0; i < S; ++i) mbar_init(&full_bar[i], 1);
         abort_s = 0;
         mbar_fence_init();
-        for (; issued < min(S, nst); ++issued) issue(issued);
+        // the first ring fill does not depend on the previous kernel -- unless
+        // that kernel wrote this step's keys (rows may share pages)
+        if (!p.kv_prewritten)
+            for (; issued < min(S, nst); ++issued) issue(issued);
         tr = trace_if_on(p.trace);   // after the copies: the enable word is a global load
         trace_mark(tr, p.trace_id, 0);
     }
     __syncthreads();
 
     pdl_wait();
-    if (tid == 0) trace_mark(tr, p.trace_id, 1);
+    if (tid == 0) {
+        for (; issued < min(S, nst); ++issued) issue(issued);
+        trace_mark(tr, p.trace_id, 1);
+    }
     int pos = p.pos[r];
     pos = min(max(pos, 0), p.cap - 1);   // an out-of-range pos was flagged by the embedding kernel
     const float* qrow = p.qkv + (size_t)r * p.qkv_stride;
@@ -146,7 +152,7 @@ __global__ void __launch_bounds__(AM_THREADS, 2) k_attn_mma(const __grid_constan
         q_s[h * HD + d] = (a * cs.x - b * cs.y) * p.scale;
         q_s[h * HD + d + HD / 2] = (a * cs.y + b * cs.x) * p.scale;
     }
-    const bool owner = pos >= j0 && pos < j1;
+    const bool owner = !p.kv_prewritten && pos >= j0 && pos < j1;
     if (owner) {
         const float* kh = qrow + (size_t)p.Hq * HD + (size_t)g * HD;
         const float* vh = kh + (size_t)p.Hkv * HD;
@@ -415,6 +421,59 @@ __global__ void __launch_bounds__(AM_THREADS, 2) k_attn_mma(const __grid_constan
 }
 
 // ---------------- host side ----------------
+
+// The K/V write of every row as its own kernel, so that rows which share
+// pages (the chunk of a multi-token prefill: row t is position pos0 + t of one
+// sequence) all see each other's new keys.  One CTA per (kv head, row);
+// arithmetic identical to the in-kernel write of k_attn_mma.
+__global__ void __launch_bounds__(128) k_kv_write(const AttnParams p) {
+    const int g = blockIdx.x, r = blockIdx.y, tid = threadIdx.x;
+    const int HD = p.hd;
+    pdl_wait();
+    int pos = p.pos[r];
+    pos = min(max(pos, 0), p.cap - 1);   // an out-of-range pos was flagged by the embedding kernel
+    const float* kh = p.qkv + (size_t)r * p.qkv_stride + (size_t)p.Hq * HD + (size_t)g * HD;
+    const float* vh = kh + (size_t)p.Hkv * HD;
+    const float2* rt = p.rope + (size_t)pos * (HD / 2);
+    size_t off;
+    if (p.page_size > 0 && p.write_map && p.slot_map) {
+        const int P = p.page_size;
+        const int slot = p.write_map[r];
+        if (slot < 0 || slot >= p.num_pages * P) {
+            if (tid == 0) atomicOr(p.err, FAULT_WRITE_MAP);
+            pdl_trigger();
+            return;
+        }
+        off = (((size_t)(slot / P) * p.Hkv + g) * P + slot % P) * HD;
+    } else {
+        off = (((size_t)r * p.Hkv + g) * p.cap + pos) * HD;
+    }
+    __nv_bfloat16* Kc = reinterpret_cast<__nv_bfloat16*>(p.Kc);
+    __nv_bfloat16* Vc = reinterpret_cast<__nv_bfloat16*>(p.Vc);
+    for (int d = tid; d < HD / 2; d += blockDim.x) {
+        const float a = kh[d], b = kh[d + HD / 2];
+        const float2 cs = rt[d];
+        Elem<__nv_bfloat16>::round_store(a * cs.x - b * cs.y, Kc + off + d);
+        Elem<__nv_bfloat16>::round_store(a * cs.y + b * cs.x, Kc + off + d + HD / 2);
+    }
+    for (int d = tid; d < HD; d += blockDim.x) Elem<__nv_bfloat16>::round_store(vh[d], Vc + off + d);
+    pdl_trigger();
+}
+
+cudaError_t kv_write_launch(const AttnPlan& plan, cudaStream_t s, bool pdl) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(plan.p.Hkv, plan.p.R);
+    cfg.blockDim = dim3(128);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    AttnParams p = plan.p;
+    void* args[] = {&p};
+    return cudaLaunchKernelExC(&cfg, (const void*)&k_kv_write, args);
+}
 
 template <int HD, int G>
 static const void* am_pick_paged(bool paged) {

@@ -129,6 +129,7 @@ struct dec_handle {
     bool own_stream = false;
     char* ws = nullptr;
     bool own_ws = false;
+    int extra_kernels = 0;         // recorded kernels without a trace slot (K/V writes before attention)
     WsLayout lay{};
     StatusBlock* d_status = nullptr;
     int32_t* d_slots = nullptr;
@@ -281,6 +282,10 @@ std::vector<float2> rope_table(int cap, int hd, double theta) {
 }
 
 cudaError_t launch_attn(const AttnPlan& a, cudaStream_t s, bool pdl) {
+    if (a.prewrite) {
+        cudaError_t e = kv_write_launch(a, s, pdl);
+        if (e != cudaSuccess) return e;
+    }
     return a.mma ? attn_mma_launch(a, s, pdl) : attn_launch(a, s, pdl);
 }
 
@@ -647,6 +652,12 @@ int dec_capture(dec_handle* h, int32_t cap, int32_t rows, int32_t kv_layout, int
             if ((e = attn_mma_plan(&ap, h->num_sms)) != cudaSuccess)
                 return fail(h, DEC_E_UNSUPPORTED, "no attention kernel for head_dim=%d group=%d cap=%d (%s)", hd,
                             Hq / Hkv, cap, cudaGetErrorString(e));
+            // several rows: every row's K/V lands before any row's attention, so
+            // rows may share pages (a multi-token prefill chunk of one sequence)
+            if (rows >= 2) {
+                ap.prewrite = true;
+                ap.p.kv_prewritten = 1;
+            }
             continue;
         }
         if ((e = attn_plan(&ap, h->num_sms)) != cudaSuccess)
@@ -654,6 +665,7 @@ int dec_capture(dec_handle* h, int32_t cap, int32_t rows, int32_t kv_layout, int
                         Hq / Hkv, cap, cudaGetErrorString(e));
     }
     h->kernels = kernels_per_step(c.n_layers);
+    h->extra_kernels = (!h->attn.empty() && h->attn[0].prewrite) ? c.n_layers : 0;
     if ((e = cudaMemsetAsync(h->d_trace, 0, sizeof(unsigned long long), h->stream)) != cudaSuccess)
         return cuda_fail(h, e, "trace clear");
     if (h->strategy == DEC_STRATEGY_PERSISTENT) {
@@ -873,6 +885,62 @@ int dec_chain(dec_handle* h, int32_t n_steps, const int32_t* tokens, const int32
     return DEC_OK;
 }
 
+int dec_prefill(dec_handle* h, const int32_t* pages, const int32_t* tokens, int32_t n, int32_t pos0, float* logits_out,
+                int32_t* id_out) {
+    int rc = gate(h, true);
+    if (rc) return rc;
+    if (h->state == ST_NEEDS_RESET) return fail(h, DEC_E_NEEDS_RESET, "an earlier step failed; call dec_reset_state");
+    if (h->layout != DEC_KV_PAGED || h->rows < 2 || h->strategy != DEC_STRATEGY_GRAPH || h->attn.empty() ||
+        !h->attn[0].prewrite)
+        return fail(h, DEC_E_UNSUPPORTED, "multi-token prefill needs a paged graph capture of 2..8 rows with bf16 K/V");
+    if (!pages || !tokens) return fail(h, DEC_E_INVALID, "pages and tokens are required");
+    if (n < 1 || pos0 < 0 || (int64_t)pos0 + n > h->cap)
+        return fail(h, DEC_E_RANGE, "positions [%d, %d) outside [0, %d)", pos0, pos0 + n, h->cap);
+    for (int i = 0; i < h->ppr; ++i)
+        if (pages[i] < 0 || pages[i] >= h->npages)
+            return fail(h, DEC_E_RANGE, "pages[%d] = %d outside [0, %d)", i, pages[i], h->npages);
+    for (int i = 0; i < n; ++i)
+        if (tokens[i] < 0 || tokens[i] >= h->cfg.vocab)
+            return fail(h, DEC_E_RANGE, "tokens[%d] = %d outside [0, %d)", i, tokens[i], h->cfg.vocab);
+    const int R = h->rows;
+    // every row reads and writes this sequence's pages for the duration of the prefill
+    std::vector<int32_t> shared((size_t)R * h->ppr);
+    for (int r = 0; r < R; ++r) memcpy(shared.data() + (size_t)r * h->ppr, pages, sizeof(int32_t) * h->ppr);
+    cudaError_t e = cudaMemcpyAsync(h->d_slot_map, shared.data(), shared.size() * sizeof(int32_t),
+                                    cudaMemcpyHostToDevice, h->stream);
+    if (e != cudaSuccess) return cuda_fail(h, e, "slot map write");
+    std::vector<float> last;
+    int32_t ids[MAX_ROWS];
+    int last_row = 0;
+    for (int c = 0; c < n && rc == DEC_OK; c += R) {
+        const int m = std::min(R, n - c);
+        // rows past the chunk repeat its last token: same position, same bytes written
+        for (int r = 0; r < R; ++r) {
+            const int t = c + std::min(r, m - 1), p = pos0 + t;
+            h->h_slots[r] = tokens[t];
+            h->h_slots[R + r] = p;
+            h->h_slots[2 * R + r] = pages[p / h->page] * h->page + p % h->page;
+        }
+        if ((e = cudaMemcpyAsync(h->d_slots, h->h_slots, 3 * sizeof(int32_t) * R, cudaMemcpyHostToDevice, h->stream)) !=
+            cudaSuccess)
+            return cuda_fail(h, e, "slot write");
+        if ((rc = launch_step(h)) != DEC_OK) return rc;
+        const bool final_chunk = c + R >= n;
+        if (final_chunk && logits_out) last.resize((size_t)R * h->cfg.vocab);
+        rc = finish_step(h, final_chunk && logits_out ? last.data() : nullptr, ids, nullptr);
+        last_row = m - 1;
+    }
+    // the caller's page table again
+    e = cudaMemcpyAsync(h->d_slot_map, h->slot_map_host.data(), h->slot_map_host.size() * sizeof(int32_t),
+                        cudaMemcpyHostToDevice, h->stream);
+    if (e != cudaSuccess) return cuda_fail(h, e, "slot map restore");
+    if (rc != DEC_OK) return rc;
+    if ((rc = bounded_wait(h)) != DEC_OK) return rc;
+    if (logits_out) memcpy(logits_out, last.data() + (size_t)last_row * h->cfg.vocab, sizeof(float) * h->cfg.vocab);
+    if (id_out) *id_out = ids[last_row];
+    return DEC_OK;
+}
+
 int dec_set_strategy(dec_handle* h, int32_t strategy) {
     int rc = gate(h, false);
     if (rc) return rc;
@@ -938,7 +1006,7 @@ int dec_stats_get(const dec_handle* h, dec_stats* out) {
     out->steps = h->steps;
     out->replays = h->replays;
     out->eager_steps = h->eager_steps;
-    out->kernels_per_step = h->strategy == DEC_STRATEGY_PERSISTENT ? 1 : h->kernels;
+    out->kernels_per_step = h->strategy == DEC_STRATEGY_PERSISTENT ? 1 : h->kernels + h->extra_kernels;
     out->graph_nodes = (int32_t)h->nodes;
     out->attn_splits = h->strategy == DEC_STRATEGY_PERSISTENT ? h->persist.p.nsplit
                                                               : (h->attn.empty() ? 0 : h->attn[0].p.nsplit);

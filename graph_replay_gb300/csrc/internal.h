@@ -95,6 +95,7 @@ struct AttnParams {
     unsigned* counters;    // [R, Hkv] split-completion counters (zero between steps)
     float* out;            // [R, Hq * hd]
     unsigned* err;
+    int kv_prewritten;     // 1: every row's new k, v are already in the store (k_kv_write ran)
     float scale;
     unsigned long long* trace;
     int trace_id;
@@ -110,7 +111,12 @@ struct AttnPlan {
     AttnParams p;
     bool mma = false;              // tensor-core kernel (attn_mma.cu)
     void* mma_params = nullptr;    // its parameter block (tensor maps + p), owned by the plan
+    bool prewrite = false;         // launch k_kv_write before the attention (p.kv_prewritten = 1)
 };
+
+// RoPE of every row's k at Pos, rounding and store of k, v (bf16 store) at the
+// row's position or WriteMap slot, before the attention of any row reads them
+cudaError_t kv_write_launch(const AttnPlan& plan, cudaStream_t s, bool pdl);
 
 // choose split_len / nsplit; returns cudaErrorInvalidValue for unsupported head_dim / group
 cudaError_t attn_plan(AttnPlan* plan, int num_sms);

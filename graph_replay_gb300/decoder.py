@@ -130,6 +130,17 @@ class Decoder:
         B.check(self.h, B.dec_chain(self.h, int(n_steps), _ptr(tok), _ptr(ps), _ptr(ids), _ptr(nf)))
         return ids, nf
 
+    def prefill(self, pages, tokens, pos0: int = 0):
+        """Multi-token prefill of one sequence through the paged step (rows tokens
+        per chunk): returns (logits [vocab] after the last token, greedy id)."""
+        pg = np.ascontiguousarray(pages, dtype=np.int32).reshape(-1)
+        tk = np.ascontiguousarray(tokens, dtype=np.int32).reshape(-1)
+        logits = np.empty(self.vocab, dtype=np.float32)
+        idv = np.zeros(1, dtype=np.int32)
+        self._after_torch()
+        B.check(self.h, B.dec_prefill(self.h, _ptr(pg), _ptr(tk), int(tk.size), int(pos0), _ptr(logits), _ptr(idv)))
+        return logits, int(idv[0])
+
     def launch(self, dev_slots: Optional[torch.Tensor]) -> None:
         """Asynchronous step from a device slot record [3*rows] int32 (tokens, pos, write map)."""
         self._after_torch()

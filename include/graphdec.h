@@ -253,6 +253,27 @@ int dec_wait(dec_handle *h, float *logits_out, int32_t *ids_out, uint8_t *nonfin
 int dec_chain(dec_handle *h, int32_t n_steps, const int32_t *tokens, const int32_t *pos, int32_t *ids_out,
               uint8_t *nonfinite_out);
 
+/* Multi-token prefill of ONE sequence ("Models, Registry and the Driver",
+ * section "The Model": a step shape is rows x new tokens; positions are
+ * absolute, so a prefill is a step continuing from a position).  The n tokens
+ * at positions pos0 .. pos0 + n - 1 run through the recorded paged step in
+ * chunks of `rows` tokens: in each chunk row t is position pos0 + c + t of the
+ * sequence, every row reads and writes the sequence's pages, and every row's
+ * K/V is stored before any row's attention reads the pages.  Afterwards the
+ * sequence's K/V for those positions is in its pages, and the caller's slot
+ * map is in place again.
+ *   pages       host [cap / page_size] page ids of the sequence, each in
+ *               [0, num_pages)
+ *   tokens      host [n], each in [0, vocab)
+ *   pos0        first position; pos0 + n <= cap (DEC_E_RANGE otherwise)
+ *   logits_out  host [vocab] fp32 logits after the last token, or NULL
+ *   id_out      host, the greedy id after the last token, or NULL
+ * Needs a paged graph capture of 2..8 rows with bf16 K/V (DEC_E_UNSUPPORTED
+ * otherwise).  Per token the arithmetic equals a decode step of that token, so
+ * the chunking does not change any result. */
+int dec_prefill(dec_handle *h, const int32_t *pages, const int32_t *tokens, int32_t n, int32_t pos0,
+                float *logits_out, int32_t *id_out);
+
 /* Choose the execution strategy (dec_strategy) for the coming dec_capture;
  * DEC_E_STATE after capture.  Default DEC_STRATEGY_GRAPH. */
 int dec_set_strategy(dec_handle *h, int32_t strategy);
