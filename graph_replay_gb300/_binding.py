@@ -77,6 +77,8 @@ _SIG = [
     ("dec_wait", ctypes.c_int, [_P, _P, _P, _P]),
     ("dec_chain", ctypes.c_int, [_P, _I32, _P, _P, _P, _P]),
     ("dec_prefill", ctypes.c_int, [_P, _P, _P, _I32, _I32, _P, _P]),
+    ("dec_set_sampler", ctypes.c_int, [_P, _P]),
+    ("dec_logprobs", ctypes.c_int, [_P, _I32, _P, _P]),
     ("dec_set_strategy", ctypes.c_int, [_P, _I32]),
     ("dec_set_eager", ctypes.c_int, [_P, _I32]),
     ("dec_reset_state", ctypes.c_int, [_P]),
@@ -194,6 +196,24 @@ def dec_chain(h, n_steps: int, tokens_ptr, pos_ptr, ids_ptr, nonfinite_ptr) -> i
 
 
 DEC_CHAIN_MAX_STEPS = 4096
+
+
+class dec_sampler(ctypes.Structure):
+    _fields_ = [("temperature", ctypes.c_float), ("top_k", ctypes.c_int32), ("top_p", ctypes.c_float),
+                ("min_p", ctypes.c_float), ("seed", ctypes.c_uint64), ("n_logprobs", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+DEC_SAMPLER_MAX_TOP_K = 1024
+DEC_LOGPROBS_MAX = 8
+
+
+def dec_set_sampler(h, sampler) -> int:
+    return lib().dec_set_sampler(h, None if sampler is None else ctypes.byref(sampler))
+
+
+def dec_logprobs(h, n: int, ids_ptr, vals_ptr) -> int:
+    return lib().dec_logprobs(h, n, ids_ptr, vals_ptr)
 
 
 def dec_prefill(h, pages_ptr, tokens_ptr, n: int, pos0: int, logits_ptr, id_ptr) -> int:

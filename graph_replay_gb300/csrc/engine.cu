@@ -37,11 +37,18 @@ constexpr int CHAIN_MAX = DEC_CHAIN_MAX_STEPS;   // steps one dec_chain call rec
 constexpr size_t ALIGN = 256;
 
 // per-step status block read back after every step (one copy)
+static_assert(sizeof(dec_sampler) == sizeof(SamplerSlot), "the sampler slot mirrors dec_sampler");
+static_assert(offsetof(dec_sampler, seed) == offsetof(SamplerSlot, seed), "the sampler slot mirrors dec_sampler");
+static_assert(offsetof(dec_sampler, n_logprobs) == offsetof(SamplerSlot, n_logprobs), "the sampler slot mirrors dec_sampler");
+
 struct StatusBlock {
     unsigned err;
     unsigned pad;
     unsigned long long amax[MAX_ROWS];
     unsigned nonfinite[MAX_ROWS];
+    int sampled[MAX_ROWS];                        // sampling suffix: the picks
+    int lp_ids[MAX_ROWS * DEC_LOGPROBS_MAX];      // top-n logprob ids
+    float lp_vals[MAX_ROWS * DEC_LOGPROBS_MAX];   // and values
 };
 
 size_t align_up(size_t v) { return (v + ALIGN - 1) / ALIGN * ALIGN; }
@@ -51,7 +58,7 @@ int es_of(int dtype) { return dtype == DEC_DTYPE_BF16 ? 2 : 4; }
 // Offsets of every buffer of a capture inside one workspace.
 struct WsLayout {
     size_t status, slots, slot_map, counters, trace, ptabs, tmaps, gbar, x, qkv, attn, gu, logits, part, gpart, gcnt,
-        chain, rope, kv, kv_layer, total;
+        chain, sampler, rope, kv, kv_layer, total;
 };
 
 // kernels recorded per step: embedding, 5 per layer, head
@@ -91,6 +98,7 @@ bool compute_layout(const dec_config& c, int cap, int R, int layout, int page, i
     L->gcnt = take(gp ? GEMV_TC_CNT_WORDS * sizeof(unsigned) : 0);
     // chained steps: counter, sticky error word, id and flag histories
     L->chain = take(2 * sizeof(int) + 2 * (size_t)CHAIN_MAX * R * sizeof(int));
+    L->sampler = take(sizeof(SamplerSlot));
     L->rope = take((size_t)cap * (hd / 2) * sizeof(float2));
     const size_t es = (size_t)es_of(c.kv_dtype);
     if (layout == DEC_KV_PAGED)
@@ -129,7 +137,9 @@ struct dec_handle {
     bool own_stream = false;
     char* ws = nullptr;
     bool own_ws = false;
-    int extra_kernels = 0;         // recorded kernels without a trace slot (K/V writes before attention)
+    int extra_kernels = 0;         // recorded kernels without a trace slot (K/V writes, sampling)
+    bool sampler_on = false;       // the sampling kernel is (to be) recorded after the head
+    dec_sampler sampler{};         // its parameters
     WsLayout lay{};
     StatusBlock* d_status = nullptr;
     int32_t* d_slots = nullptr;
@@ -291,17 +301,36 @@ cudaError_t launch_attn(const AttnPlan& a, cudaStream_t s, bool pdl) {
 
 // launch the whole step (the sequence the graph records)
 cudaError_t enqueue_step(dec_handle* h) {
-    if (h->strategy == DEC_STRATEGY_PERSISTENT) return persist_launch(h->persist, h->stream);
-    cudaError_t e = embed_launch(h->cfg.weight_dtype == DEC_DTYPE_BF16 ? W_BF16 : W_F32, h->embed_p, h->stream);
-    if (e != cudaSuccess) return e;
-    for (int l = 0; l < h->cfg.n_layers; ++l) {
-        if ((e = gemv_launch(h->gemv[4 * l + 0], h->stream, h->pdl)) != cudaSuccess) return e;
-        if ((e = launch_attn(h->attn[l], h->stream, h->pdl)) != cudaSuccess) return e;
-        if ((e = gemv_launch(h->gemv[4 * l + 1], h->stream, h->pdl)) != cudaSuccess) return e;
-        if ((e = gemv_launch(h->gemv[4 * l + 2], h->stream, h->pdl)) != cudaSuccess) return e;
-        if ((e = gemv_launch(h->gemv[4 * l + 3], h->stream, h->pdl)) != cudaSuccess) return e;
+    cudaError_t e;
+    if (h->strategy == DEC_STRATEGY_PERSISTENT) {
+        if ((e = persist_launch(h->persist, h->stream)) != cudaSuccess) return e;
+    } else {
+        if ((e = embed_launch(h->cfg.weight_dtype == DEC_DTYPE_BF16 ? W_BF16 : W_F32, h->embed_p, h->stream)) !=
+            cudaSuccess)
+            return e;
+        for (int l = 0; l < h->cfg.n_layers; ++l) {
+            if ((e = gemv_launch(h->gemv[4 * l + 0], h->stream, h->pdl)) != cudaSuccess) return e;
+            if ((e = launch_attn(h->attn[l], h->stream, h->pdl)) != cudaSuccess) return e;
+            if ((e = gemv_launch(h->gemv[4 * l + 1], h->stream, h->pdl)) != cudaSuccess) return e;
+            if ((e = gemv_launch(h->gemv[4 * l + 2], h->stream, h->pdl)) != cudaSuccess) return e;
+            if ((e = gemv_launch(h->gemv[4 * l + 3], h->stream, h->pdl)) != cudaSuccess) return e;
+        }
+        if ((e = gemv_launch(h->gemv.back(), h->stream, h->pdl)) != cudaSuccess) return e;
     }
-    return gemv_launch(h->gemv.back(), h->stream, h->pdl);
+    if (h->sampler_on) {
+        SampleParams sp{};
+        sp.logits = h->d_logits;
+        sp.V = h->cfg.vocab;
+        sp.R = h->rows;
+        sp.amax = h->d_status->amax;
+        sp.pos = h->d_slots + h->rows;
+        sp.cfg = reinterpret_cast<const SamplerSlot*>(h->ws + h->lay.sampler);
+        sp.sampled = h->d_status->sampled;
+        sp.lp_ids = h->d_status->lp_ids;
+        sp.lp_vals = h->d_status->lp_vals;
+        if ((e = sample_launch(sp, h->stream)) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 cudaError_t zero_state(dec_handle* h) {
@@ -360,7 +389,8 @@ int finish_step(dec_handle* h, float* logits_out, int32_t* ids_out, uint8_t* non
     for (int r = 0; r < h->rows; ++r) {
         if (ids_out) {
             const unsigned long long k = h->h_status->amax[r];
-            ids_out[r] = k ? (int32_t)(0xFFFFFFFFu - (uint32_t)(k & 0xFFFFFFFFull)) : -1;
+            ids_out[r] = h->sampler_on ? h->h_status->sampled[r]
+                                       : (k ? (int32_t)(0xFFFFFFFFu - (uint32_t)(k & 0xFFFFFFFFull)) : -1);
         }
         if (nonfinite_out) nonfinite_out[r] = h->h_status->nonfinite[r] ? 1 : 0;
     }
@@ -665,7 +695,7 @@ int dec_capture(dec_handle* h, int32_t cap, int32_t rows, int32_t kv_layout, int
                         Hq / Hkv, cap, cudaGetErrorString(e));
     }
     h->kernels = kernels_per_step(c.n_layers);
-    h->extra_kernels = (!h->attn.empty() && h->attn[0].prewrite) ? c.n_layers : 0;
+    h->extra_kernels = ((!h->attn.empty() && h->attn[0].prewrite) ? c.n_layers : 0) + (h->sampler_on ? 1 : 0);
     if ((e = cudaMemsetAsync(h->d_trace, 0, sizeof(unsigned long long), h->stream)) != cudaSuccess)
         return cuda_fail(h, e, "trace clear");
     if (h->strategy == DEC_STRATEGY_PERSISTENT) {
@@ -709,6 +739,11 @@ int dec_capture(dec_handle* h, int32_t cap, int32_t rows, int32_t kv_layout, int
         if ((e = cudaMemcpy(h->ws + L.tmaps, tm.data(), tm.size(), cudaMemcpyHostToDevice)) != cudaSuccess)
             return cuda_fail(h, e, "tensor map upload");
     }
+
+    // the sampler's parameter slot (read by the recorded sampling kernel)
+    if (h->sampler_on &&
+        (e = cudaMemcpy(h->ws + L.sampler, &h->sampler, sizeof(SamplerSlot), cudaMemcpyHostToDevice)) != cudaSuccess)
+        return cuda_fail(h, e, "sampler upload");
 
     // ---- one eager step (launch checks), then a clean state ----
     if ((e = zero_state(h)) != cudaSuccess) return cuda_fail(h, e, "state clear");
@@ -853,6 +888,7 @@ int dec_chain(dec_handle* h, int32_t n_steps, const int32_t* tokens, const int32
     cp.amax = h->d_status->amax;
     cp.nonfinite = h->d_status->nonfinite;
     cp.err = &h->d_status->err;
+    cp.sampled = h->sampler_on ? h->d_status->sampled : nullptr;
     cp.counter = d_chain;
     cp.chain_err = reinterpret_cast<unsigned*>(d_chain + 1);
     cp.ids = d_chain + 2;
@@ -941,6 +977,51 @@ int dec_prefill(dec_handle* h, const int32_t* pages, const int32_t* tokens, int3
     return DEC_OK;
 }
 
+int dec_set_sampler(dec_handle* h, const dec_sampler* sp) {
+    int rc = gate(h, false);
+    if (rc) return rc;
+    if (sp) {
+        if (!(sp->temperature >= 0.f) || !std::isfinite(sp->temperature))
+            return fail(h, DEC_E_INVALID, "temperature must be finite and >= 0");
+        if (sp->temperature > 0.f && (sp->top_k < 1 || sp->top_k > DEC_SAMPLER_MAX_TOP_K))
+            return fail(h, DEC_E_INVALID, "top_k must be in [1, %d] when sampling", DEC_SAMPLER_MAX_TOP_K);
+        if (!(sp->top_p > 0.f && sp->top_p <= 1.f)) return fail(h, DEC_E_INVALID, "top_p must be in (0, 1]");
+        if (!(sp->min_p >= 0.f && sp->min_p < 1.f)) return fail(h, DEC_E_INVALID, "min_p must be in [0, 1)");
+        if (sp->n_logprobs < 0 || sp->n_logprobs > DEC_LOGPROBS_MAX)
+            return fail(h, DEC_E_INVALID, "n_logprobs must be in [0, %d]", DEC_LOGPROBS_MAX);
+    }
+    if (!h->captured) {
+        h->sampler_on = sp != nullptr;
+        if (sp) h->sampler = *sp;
+        return DEC_OK;
+    }
+    if (!h->sampler_on) return fail(h, DEC_E_STATE, "no sampler was recorded: set one before dec_capture");
+    if (h->state == ST_POISONED) return fail(h, DEC_E_POISONED, "handle is poisoned");
+    dec_sampler v{};
+    v.top_k = 1;
+    v.top_p = 1.f;
+    if (sp) v = *sp;
+    h->sampler = v;
+    cudaError_t e = cudaMemcpyAsync(h->ws + h->lay.sampler, &h->sampler, sizeof(SamplerSlot), cudaMemcpyHostToDevice,
+                                    h->stream);
+    if (e != cudaSuccess) return cuda_fail(h, e, "sampler write");
+    return bounded_wait(h);   // the host copy may change as soon as this returns
+}
+
+int dec_logprobs(dec_handle* h, int32_t n, int32_t* ids_out, float* logprobs_out) {
+    int rc = gate(h, true);
+    if (rc) return rc;
+    if (!h->sampler_on || n < 1 || n > h->sampler.n_logprobs || !ids_out || !logprobs_out)
+        return fail(h, DEC_E_INVALID, "n = %d: at most the sampler's n_logprobs (%d)", n,
+                    h->sampler_on ? h->sampler.n_logprobs : 0);
+    for (int r = 0; r < h->rows; ++r)
+        for (int j = 0; j < n; ++j) {
+            ids_out[r * n + j] = h->h_status->lp_ids[r * DEC_LOGPROBS_MAX + j];
+            logprobs_out[r * n + j] = h->h_status->lp_vals[r * DEC_LOGPROBS_MAX + j];
+        }
+    return DEC_OK;
+}
+
 int dec_set_strategy(dec_handle* h, int32_t strategy) {
     int rc = gate(h, false);
     if (rc) return rc;
@@ -1006,7 +1087,8 @@ int dec_stats_get(const dec_handle* h, dec_stats* out) {
     out->steps = h->steps;
     out->replays = h->replays;
     out->eager_steps = h->eager_steps;
-    out->kernels_per_step = h->strategy == DEC_STRATEGY_PERSISTENT ? 1 : h->kernels + h->extra_kernels;
+    out->kernels_per_step =
+        h->strategy == DEC_STRATEGY_PERSISTENT ? 1 + (h->sampler_on ? 1 : 0) : h->kernels + h->extra_kernels;
     out->graph_nodes = (int32_t)h->nodes;
     out->attn_splits = h->strategy == DEC_STRATEGY_PERSISTENT ? h->persist.p.nsplit
                                                               : (h->attn.empty() ? 0 : h->attn[0].p.nsplit);

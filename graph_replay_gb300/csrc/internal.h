@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
+#include "graphdec.h"
 
 namespace gd {
 
@@ -144,6 +145,28 @@ struct EmbedParams {
 };
 cudaError_t embed_launch(int wtype, const EmbedParams& p, cudaStream_t s);
 
+// ---------------- sampling suffix ----------------
+struct SamplerSlot {                 // device copy of dec_sampler (same field order)
+    float temperature;
+    int top_k;
+    float top_p;
+    float min_p;
+    unsigned long long seed;
+    int n_logprobs;
+    int reserved;
+};
+struct SampleParams {
+    const float* logits;             // [R, V]
+    int V, R;
+    const unsigned long long* amax;  // [R] greedy keys
+    const int* pos;                  // [R] Pos slot (the uniform's counter)
+    const SamplerSlot* cfg;          // parameter slot
+    int* sampled;                    // [R] picks
+    int* lp_ids;                     // [R, DEC_LOGPROBS_MAX]
+    float* lp_vals;                  // [R, DEC_LOGPROBS_MAX]
+};
+cudaError_t sample_launch(const SampleParams& p, cudaStream_t s);
+
 // ---------------- chained greedy steps ----------------
 struct ChainParams {
     int* tok;                        // [R] Token slot
@@ -155,6 +178,7 @@ struct ChainParams {
     const unsigned* nonfinite;       // [R]
     unsigned* err;                   // the step's error word
     unsigned* chain_err;             // sticky over the chain
+    const int* sampled;              // [R] sampled ids, or null: greedy keys
     int* counter;                    // steps recorded so far
     int* ids;                        // [max_steps, R] history
     int* nf;                         // [max_steps, R] history

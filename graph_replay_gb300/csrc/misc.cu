@@ -84,7 +84,7 @@ __global__ void __launch_bounds__(32) k_chain_advance(const ChainParams p) {
     }
     if (r < p.R && i < p.max_steps) {
         const unsigned long long k = p.amax[r];
-        int id = k ? (int)(0xFFFFFFFFu - (unsigned)(k & 0xFFFFFFFFull)) : -1;
+        int id = p.sampled ? p.sampled[r] : (k ? (int)(0xFFFFFFFFu - (unsigned)(k & 0xFFFFFFFFull)) : -1);
         if (id < 0 || id >= p.V) {
             atomicOr(p.chain_err, FAULT_TOKEN);
             id = 0;

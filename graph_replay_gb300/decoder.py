@@ -44,6 +44,14 @@ def make_config(n_layers, d_model, n_heads, n_kv_heads, head_dim, ffn_hidden, vo
                         float(rms_eps), float(rope_theta), int(wait_timeout_ms))
 
 
+def make_sampler(temperature: float = 0.0, top_k: int = 1, top_p: float = 1.0, min_p: float = 0.0, seed: int = 0,
+                 n_logprobs: int = 0) -> B.dec_sampler:
+    s = B.dec_sampler()
+    s.temperature, s.top_k, s.top_p, s.min_p = float(temperature), int(top_k), float(top_p), float(min_p)
+    s.seed, s.n_logprobs = int(seed) & 0xFFFFFFFFFFFFFFFF, int(n_logprobs)
+    return s
+
+
 def _ptr(a: Optional[np.ndarray]):
     return None if a is None else a.ctypes.data
 
@@ -53,7 +61,7 @@ class Decoder:
 
     def __init__(self, cfg: B.dec_config, weights: dict, cap: int, rows: int = 1, kv_layout: str = "contiguous",
                  page_size: int = 16, num_pages: int = 0, stream: Optional[torch.cuda.Stream] = None,
-                 lib_workspace: bool = False, strategy: str = "graph"):
+                 lib_workspace: bool = False, strategy: str = "graph", sampler: Optional[dict] = None):
         self.cfg = cfg
         self.rows, self.cap = rows, cap
         self.layout = B.DEC_KV_PAGED if kv_layout == "paged" else B.DEC_KV_CONTIGUOUS
@@ -64,6 +72,8 @@ class Decoder:
         try:
             B.dec_load_weights(self.h, self._bindings(weights))
             B.dec_set_strategy(self.h, B.DEC_STRATEGY_PERSISTENT if strategy == "persistent" else B.DEC_STRATEGY_GRAPH)
+            if sampler is not None:   # records the sampling kernel after the head
+                B.check(self.h, B.dec_set_sampler(self.h, make_sampler(**sampler)))
             self.ws = None
             ws_ptr, ws_bytes = None, 0
             if not lib_workspace:
@@ -140,6 +150,18 @@ class Decoder:
         self._after_torch()
         B.check(self.h, B.dec_prefill(self.h, _ptr(pg), _ptr(tk), int(tk.size), int(pos0), _ptr(logits), _ptr(idv)))
         return logits, int(idv[0])
+
+    def set_sampler(self, **params) -> None:
+        """New sampler parameters for the coming steps (the decoder must have been
+        built with a sampler); see make_sampler for the fields."""
+        B.check(self.h, B.dec_set_sampler(self.h, make_sampler(**params)))
+
+    def logprobs(self, n: int):
+        """Top-n logprobs of the last step: (ids [rows, n], logprobs [rows, n])."""
+        ids = np.empty((self.rows, n), dtype=np.int32)
+        vals = np.empty((self.rows, n), dtype=np.float32)
+        B.check(self.h, B.dec_logprobs(self.h, int(n), _ptr(ids), _ptr(vals)))
+        return ids, vals
 
     def launch(self, dev_slots: Optional[torch.Tensor]) -> None:
         """Asynchronous step from a device slot record [3*rows] int32 (tokens, pos, write map)."""

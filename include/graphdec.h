@@ -274,6 +274,44 @@ int dec_chain(dec_handle *h, int32_t n_steps, const int32_t *tokens, const int32
 int dec_prefill(dec_handle *h, const int32_t *pages, const int32_t *tokens, int32_t n, int32_t pos0,
                 float *logits_out, int32_t *id_out);
 
+/* Sampling suffix beyond greedy ("Models, Registry and the Driver", section
+ * "The Driver": Head::Sample -- greedy or temperature / top-k / top-p /
+ * min-p, optional top-n logprobs).  For each row of a step:
+ *   candidates  the top_k tokens of largest logit (ties: lower index);
+ *   weights     q = exp((logit - max logit) / temperature);
+ *   kept        the shortest prefix of the candidates, by logit, whose weight
+ *               reaches top_p of the candidates' total, and only candidates
+ *               with q >= min_p (relative to the largest probability);
+ *   pick        inverse CDF over the kept prefix at u = the top 53 bits of
+ *               splitmix64 at counter (row << 32 | Pos[row]) of `seed`,
+ *               i.e. mix64(seed + (counter + 1) * 0x9E3779B97F4A7C15);
+ *   logprobs    logit - max - log(sum over the vocabulary of exp(logit - max))
+ *               of the n_logprobs tokens of largest logit.
+ * temperature = 0 picks the greedy id. */
+#define DEC_SAMPLER_MAX_TOP_K 1024
+#define DEC_LOGPROBS_MAX 8
+typedef struct dec_sampler {
+    float temperature;   /* >= 0; 0: greedy */
+    int32_t top_k;       /* 1 .. DEC_SAMPLER_MAX_TOP_K when temperature > 0 */
+    float top_p;         /* (0, 1]; 1: no top-p cut */
+    float min_p;         /* [0, 1); 0: no min-p cut */
+    uint64_t seed;
+    int32_t n_logprobs;  /* 0 .. DEC_LOGPROBS_MAX */
+    int32_t reserved;
+} dec_sampler;
+
+/* Before dec_capture: a non-NULL sampler records the sampling kernel after the
+ * head in the step (NULL: greedy only, nothing recorded).  After dec_capture:
+ * rewrites the sampler's parameters in place for the coming steps (a slot
+ * buffer, no re-capture); DEC_E_STATE if no sampler was recorded.  With a
+ * sampler recorded, the ids returned by dec_step / dec_wait and fed forward by
+ * dec_chain are the sampled ids.  DEC_E_INVALID for parameters out of range. */
+int dec_set_sampler(dec_handle *h, const dec_sampler *s);
+
+/* Top-n logprobs of the last completed step: ids_out and logprobs_out host
+ * [rows, n], n <= the sampler's n_logprobs (DEC_E_INVALID otherwise). */
+int dec_logprobs(dec_handle *h, int32_t n, int32_t *ids_out, float *logprobs_out);
+
 /* Choose the execution strategy (dec_strategy) for the coming dec_capture;
  * DEC_E_STATE after capture.  Default DEC_STRATEGY_GRAPH. */
 int dec_set_strategy(dec_handle *h, int32_t strategy);

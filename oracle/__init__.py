@@ -226,3 +226,55 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle full causal pass refused")
         return logits, Ks, Vs
+
+
+# ---- sampling suffix ("Models, Registry and the Driver", section "The Driver":
+# Head::Sample -- temperature, top-k, top-p, min-p, top-n logprobs).  Plain fp64
+# restatement of the definition; the uniform comes from splitmix64 (Steele, Lea
+# and Flood's SplitMix64 with Vigna's finalizer), written here from its
+# published definition. ----
+
+_M64 = (1 << 64) - 1
+
+
+def splitmix64_at(seed: int, counter: int) -> int:
+    """Output `counter` (0-based) of splitmix64 started at `seed`."""
+    z = (seed + (counter + 1) * 0x9E3779B97F4A7C15) & _M64
+    z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & _M64
+    z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & _M64
+    return z ^ (z >> 31)
+
+
+def uniform(seed: int, row: int, pos: int) -> float:
+    """The sampling uniform of (row, position): top 53 bits of output (row << 32 | pos)."""
+    return (splitmix64_at(seed & _M64, (row << 32) | pos) >> 11) * 2.0 ** -53
+
+
+def sample(logits, temperature: float, top_k: int, top_p: float = 1.0, min_p: float = 0.0, u: float = 0.0):
+    """One pick.  Returns (token, order, S, last): `order` the candidate ids by
+    (logit desc, index asc), S the inclusive sums of their weights
+    exp((l - l_max) / temperature), `last` the index in `order` of the last kept
+    candidate.  temperature == 0 is the greedy pick."""
+    l = np.asarray(logits, dtype=np.float64)
+    order = np.lexsort((np.arange(l.size), -l))            # logit desc, then index asc
+    if temperature <= 0.0:
+        return int(order[0]), order[:1], np.ones(1), 0
+    k = int(min(max(top_k, 1), l.size))
+    order = order[:k]
+    q = np.exp((l[order] - l[order[0]]) / temperature)
+    S = np.cumsum(q)
+    last_p = int(np.argmax(S >= min(top_p, 1.0) * S[-1]))   # shortest prefix reaching top_p of the mass
+    last_m = int(np.count_nonzero(q >= min_p)) - 1          # q is non-increasing along `order`
+    last = max(0, min(last_p, last_m))
+    target = u * S[last]
+    j = int(np.argmax(S[: last + 1] > target))
+    return int(order[j]), order, S, last
+
+
+def top_logprobs(logits, n: int):
+    """The n tokens of largest logit (ties: lower index) and their log softmax values."""
+    l = np.asarray(logits, dtype=np.float64)
+    order = np.lexsort((np.arange(l.size), -l))[:n]
+    m = l.max()
+    lse = m + np.log(np.sum(np.exp(l - m)))
+    return order, l[order] - lse

@@ -324,3 +324,80 @@ def test_kv_write_stores_rounded_projection_at_pos_only():
     o.step(0, 3, 7)
     changed = np.nonzero((o.K[0][0] != k1).any(axis=(1, 2)))[0]
     assert list(changed) == [7]
+
+
+# ---- sampling suffix ----
+
+def test_splitmix64_published_outputs():
+    # the first three outputs of splitmix64 started at 0, as published with the generator
+    assert [oracle.splitmix64_at(0, i) for i in range(3)] == [0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4,
+                                                               0x06C45D188009454F]
+
+
+def test_uniform_is_in_unit_interval_and_varies():
+    us = [oracle.uniform(99, r, p) for r in range(3) for p in range(200)]
+    assert all(0.0 <= u < 1.0 for u in us)
+    assert len(set(us)) == len(us)
+    assert abs(np.mean(us) - 0.5) < 0.05
+
+
+def test_sample_limits_reduce_to_greedy():
+    rng = np.random.default_rng(3)
+    l = rng.normal(size=50)
+    g = int(np.argmax(l))
+    for u in (0.0, 0.37, 0.999):
+        assert oracle.sample(l, 0.0, 10, 1.0, 0.0, u)[0] == g        # temperature 0
+        assert oracle.sample(l, 1.3, 1, 1.0, 0.0, u)[0] == g         # top_k = 1
+        assert oracle.sample(l, 1.3, 50, 1e-9, 0.0, u)[0] == g       # tiny top_p
+        assert oracle.sample(l, 1.3, 50, 1.0, 0.999, u)[0] == g      # min_p near 1
+
+
+def test_sample_top_p_and_min_p_cuts():
+    # probabilities 0.5, 0.3, 0.2 at temperature 1: cumulative 0.5, 0.8, 1.0
+    l = np.log([0.5, 0.3, 0.2])
+    for top_p, last in ((0.49, 0), (0.51, 1), (0.79, 1), (0.81, 2), (1.0, 2)):
+        assert oracle.sample(l, 1.0, 3, top_p, 0.0, 0.0)[3] == last
+    # relative probabilities 1, 0.6, 0.4
+    assert oracle.sample(l, 1.0, 3, 1.0, 0.5, 0.0)[3] == 1
+    assert oracle.sample(l, 1.0, 3, 1.0, 0.61, 0.0)[3] == 0
+    assert oracle.sample(l, 1.0, 3, 0.81, 0.39, 0.0)[3] == 2
+    assert oracle.sample(l, 1.0, 3, 0.81, 0.41, 0.0)[3] == 1
+
+
+def test_sample_frequencies_equal_the_kept_softmax():
+    # u on a fine grid: each kept token is picked for exactly its share of the grid
+    from scipy.special import softmax
+    rng = np.random.default_rng(11)
+    l = rng.normal(size=12) * 2
+    T, k, top_p, min_p, M = 0.7, 8, 0.9, 0.05, 20000
+    picks = np.array([oracle.sample(l, T, k, top_p, min_p, (i + 0.5) / M)[0] for i in range(M)])
+    order = list(np.argsort(-l, kind="stable"))[:k]
+    p = softmax(l[order] / T)
+    keep = 0
+    while np.sum(p[: keep + 1]) < top_p - 1e-12:
+        keep += 1
+    keep = min(keep, int(np.sum(p / p[0] >= min_p)) - 1)
+    want = p[: keep + 1] / np.sum(p[: keep + 1])
+    for j, tok in enumerate(order):
+        freq = np.mean(picks == tok)
+        assert abs(freq - (want[j] if j <= keep else 0.0)) <= 1.0 / M + 1e-12, (j, freq)
+
+
+def test_sample_ties_go_to_the_lower_index():
+    l = np.array([1.0, 3.0, 2.0, 3.0, 3.0])
+    tok, order, _, _ = oracle.sample(l, 1.0, 2, 1.0, 0.0, 0.99)
+    assert list(order) == [1, 3]
+    assert tok == 3
+    ids, _ = oracle.top_logprobs(l, 4)
+    assert list(ids) == [1, 3, 4, 2]
+
+
+def test_top_logprobs_closed_form():
+    from scipy.special import logsumexp
+    ids, lp = oracle.top_logprobs([0.0, np.log(3.0)], 2)
+    assert list(ids) == [1, 0]
+    assert np.allclose(lp, [np.log(0.75), np.log(0.25)], atol=1e-15)
+    rng = np.random.default_rng(5)
+    l = rng.normal(size=1000) * 3
+    ids, lp = oracle.top_logprobs(l, 5)
+    assert np.allclose(lp, l[ids] - logsumexp(l), atol=1e-12)
