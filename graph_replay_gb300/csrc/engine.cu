@@ -91,7 +91,9 @@ bool compute_layout(const dec_config& c, int cap, int R, int layout, int page, i
         const int qkv_n = (int)((Hq + 2 * Hkv) * hd);
         for (size_t need : {gemv_tc_part_floats(R, (int)d, qkv_n, false), gemv_tc_part_floats(R, (int)(Hq * hd), (int)d, false),
                             gemv_tc_part_floats(R, (int)d, (int)(2 * F), true), gemv_tc_part_floats(R, (int)F, (int)d, false),
-                            gemv_tc_part_floats(R, (int)d, (int)V, false)})
+                            gemv_tc_part_floats(R, (int)d, (int)V, false), gemv_box_part_floats(R, (int)d, qkv_n),
+                            gemv_box_part_floats(R, (int)(Hq * hd), (int)d), gemv_box_part_floats(R, (int)d, (int)(2 * F)),
+                            gemv_box_part_floats(R, (int)F, (int)d), gemv_box_part_floats(R, (int)d, (int)V)})
             gp = need > gp ? need : gp;
     }
     L->gpart = take(gp * 4);
@@ -588,11 +590,24 @@ int dec_capture(dec_handle* h, int32_t cap, int32_t rows, int32_t kv_layout, int
     // reads silu(gate) * up from the first F columns of the gate/up buffer.
     const char* gemv_env = getenv("GRAPHDEC_GEMV");
     const bool tc = wt == W_BF16 && rows >= 2 && !(gemv_env && strcmp(gemv_env, "simd") == 0);
+    // Which tensor-core GEMV streams a projection: whole-box TMA copies for large
+    // matrices (>= 96 MB of weights), one bulk copy per weight row below that,
+    // where its shorter start-up wins (measured: 8B qkv / o-proj 20.7 / 14.6 us
+    // row-copy vs 25.2 / 22.8 us box; gate/up / down / head 67.7 / 40.8 / 355 us
+    // row-copy vs 52.3 / 35.4 / 200 us box).  GRAPHDEC_GEMV=rowcopy or =box forces one.
+    const bool force_row = gemv_env && strcmp(gemv_env, "rowcopy") == 0;
+    const bool force_box = gemv_env && strcmp(gemv_env, "box") == 0;
+    auto tc_kind_for = [&](long long n, long long k) {
+        if (!tc) return 0;
+        if (force_row) return 1;
+        if (force_box) return 2;
+        return n * k * 2 >= (96ll << 20) ? 2 : 1;
+    };
     auto mk = [&](int pro, int epi, const void* w0, int n0, const void* w1, int n1, const void* w2, int n2, int K,
                   const float* act, int act_stride, const void* gain, float* out, int out_stride) {
         GemvPlan pl{};
         pl.wtype = wt;
-        pl.tc = tc ? 1 : 0;
+        pl.tc = tc_kind_for(n0 + n1 + n2, K);
         pl.pro = pro;
         pl.epi = epi;
         GemvParams& p = pl.p;
@@ -612,6 +627,7 @@ int dec_capture(dec_handle* h, int32_t cap, int32_t rows, int32_t kv_layout, int
         p.err = &h->d_status->err;
         p.trace = h->d_trace;
         p.tc_part = (float*)(h->ws + h->lay.gpart);
+        p.tc_part_cap = (h->lay.gcnt - h->lay.gpart) / sizeof(float);
         p.tc_cnt = (unsigned*)(h->ws + h->lay.gcnt);
         return pl;
     };

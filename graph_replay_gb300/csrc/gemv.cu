@@ -9,6 +9,9 @@ const void* gemv_kernel_bf16(int nr, int cpl, int pro, int epi);
 const void* gemv_kernel_f32(int nr, int cpl, int pro, int epi);
 const void* gemv_tc_kernel(int pro, int epi, int ws);
 cudaError_t gemv_tc_plan(GemvPlan* plan, int num_sms);
+const void* gemv_box_kernel(int pro, int epi);
+cudaError_t gemv_box_plan(GemvPlan* plan, int num_sms);
+cudaError_t gemv_box_launch(const GemvPlan& plan, cudaStream_t s, bool pdl);
 
 namespace {
 // mirrors gemv_impl.cuh
@@ -20,6 +23,7 @@ constexpr int MAX_S = 6;
 constexpr int MAX_RPS = 32;
 
 const void* pick(const GemvPlan& pl) {
+    if (pl.tc == 2) return gemv_box_kernel(pl.pro, pl.epi);
     if (pl.tc) return gemv_tc_kernel(pl.pro, pl.epi, pl.p.tc_ws);
     return pl.wtype == W_BF16 ? gemv_kernel_bf16(pl.nr, pl.cpl, pl.pro, pl.epi)
                               : gemv_kernel_f32(pl.nr, pl.cpl, pl.pro, pl.epi);
@@ -43,6 +47,11 @@ int cpl_for(int need, int nr, int wtype) {
 }  // namespace
 
 cudaError_t gemv_plan(GemvPlan* plan, int num_sms) {
+    if (plan->tc == 2) {
+        // box-streamed tensor-core GEMV; the row-copy one where no box plan fits
+        if (gemv_box_plan(plan, num_sms) == cudaSuccess) return cudaSuccess;
+        plan->tc = 1;
+    }
     if (plan->tc) return gemv_tc_plan(plan, num_sms);
     GemvParams& p = plan->p;
     const int vec = plan->wtype == W_BF16 ? 8 : 4;
@@ -91,6 +100,7 @@ cudaError_t gemv_plan(GemvPlan* plan, int num_sms) {
 }
 
 cudaError_t gemv_launch(const GemvPlan& plan, cudaStream_t s, bool pdl) {
+    if (plan.tc == 2) return gemv_box_launch(plan, s, pdl);
     const void* fn = pick(plan);
     if (!fn) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};

@@ -539,7 +539,9 @@ cudaError_t gemv_tc_plan(GemvPlan* plan, int num_sms) {
     int nrr = num_sms / ks;                      // row ranges
     if (nrr > nu) nrr = nu;
     if (nrr < 1 || (ks > 1 && nrr > (int)GEMV_TC_CNT_WORDS)) return cudaErrorInvalidValue;
-    if (ks > 1 && (!p.tc_part || !p.tc_cnt)) return cudaErrorInvalidValue;
+    if (ks > 1 && (!p.tc_part || !p.tc_cnt ||
+                   (size_t)ks * p.R * (size_t)p.N + (size_t)ks * nrr * 8 > p.tc_part_cap))
+        return cudaErrorInvalidValue;
     fn = gemv_tc_kernel(plan->pro, plan->epi, ws);   // same static shared memory at either width
     p.rps = TC_GT;
     p.stages = S;

@@ -54,9 +54,12 @@ struct GemvParams {
     unsigned* err;             // error word (FAULT_WAIT)
     int rps;                   // weight rows per ring stage (tensor-core GEMV: tiles per row group)
     int stages;                // ring stages
+    int tc_bh;                 // box-streamed tensor-core GEMV: rows per box (row group)
+    int tc_seg_ranges[3];      // box-streamed tensor-core GEMV: row ranges per segment
     int tc_ws;                 // tensor-core GEMV: weight columns per stage
     int tc_ks;                 // tensor-core GEMV: K splits (CTAs per row range)
     float* tc_part;            // tensor-core GEMV, tc_ks > 1: partial sums [ks][R][N or 2F] + [ks][ranges][8] sums of squares
+    size_t tc_part_cap;        // floats available at tc_part
     unsigned* tc_cnt;          // tensor-core GEMV, tc_ks > 1: arrivals per row range (zero between launches)
     unsigned long long* trace; // trace buffer or null
     int trace_id;
@@ -64,7 +67,8 @@ struct GemvParams {
 
 struct GemvPlan {
     int wtype, pro, epi, nr, cpl;
-    int tc;                // 1: tensor-core GEMV (gemv_tc.cu, bf16 weights, 1..8 rows)
+    int tc;                // 1: tensor-core GEMV (gemv_tc.cu), 2: box-streamed tensor-core GEMV (gemv_tma.cu)
+    alignas(64) unsigned char tma_maps[3 * 128];   // tc == 2: one TMA tensor map per weight segment
     int grid, block;
     size_t smem;
     GemvParams p;
@@ -75,6 +79,8 @@ cudaError_t gemv_plan(GemvPlan* plan, int num_sms);
 // Scratch of the tensor-core GEMV for rows x (K -> N) (paired: N = 2F): floats
 // of split partials, and the arrival counters (words), for any device.
 size_t gemv_tc_part_floats(int R, int K, int N, bool paired);
+// the same for the box-streamed tensor-core GEMV (it splits K up to 16 ways)
+size_t gemv_box_part_floats(int R, int K, int N);
 constexpr size_t GEMV_TC_CNT_WORDS = 1024;
 cudaError_t gemv_launch(const GemvPlan& plan, cudaStream_t s, bool pdl);
 
