@@ -107,6 +107,32 @@ def test_tensor_core_and_cuda_core_gemv_agree():
         assert_close(a, b, wl, "tensor-core vs CUDA-core GEMV")
 
 
+@pytest.mark.parametrize("mode", ["box", "rowcopy"])
+def test_each_tensor_core_gemv_matches_the_oracle(mode):
+    # every projection through one of the two tensor-core GEMVs (TMA boxes with
+    # split K, or one bulk copy per weight row), 3 rows, against the oracle
+    wl = gen.WORKLOADS["1b"].replace(name=f"1b_{mode}", n_layers=2, cap=256, rows=3)
+    old = os.environ.get("GRAPHDEC_GEMV")
+    os.environ["GRAPHDEC_GEMV"] = mode
+    try:
+        dec, mw = make_decoder(wl)
+    finally:
+        if old is None:
+            del os.environ["GRAPHDEC_GEMV"]
+        else:
+            os.environ["GRAPHDEC_GEMV"] = old
+    orcs = [oracle.Oracle(mw, cap=wl.cap) for _ in range(3)]
+    toks = [gen.prompt_tokens(wl, row=r, n=8) for r in range(3)]
+    for i in range(8):
+        pos = [i, i + 40, i + 100]
+        res = dec.step([int(toks[r][i]) for r in range(3)], pos)
+        for r in range(3):
+            ref = orcs[r].step(0, int(toks[r][i]), pos[r])
+            assert_close(res.logits[r], ref, wl, f"{mode} row {r} step {i}")
+            assert_greedy(res.ids[r], ref, f"{mode} row {r} step {i}")
+    dec.close()
+
+
 @pytest.mark.slow
 def test_8b_paged_rows8_prefilled():
     # the paged configuration at full size: 8 rows, 16-token pages in a pool of 4096, SlotMap a
