@@ -140,6 +140,21 @@ def _workload(args):
     return wl
 
 
+def max_over_ranks(x: float, world: int, device="cpu") -> float:
+    """The largest value over all ranks: a replicated job takes as long as its slowest replica."""
+    if world <= 1:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, rows: int, steps: int, seconds: float) -> float:
+    """Whole-job throughput: every replica steps `rows` sequences `steps` times."""
+    return world * rows * steps / seconds
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
 
@@ -216,12 +231,9 @@ def run_ours(args, rank, world, local_rank):
     clk = clocks.stop()
     res = dec.wait()   # the device checks of the timed steps passed
     assert res.nonfinite.sum() == 0
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
     ms_step = ms / args.steps
-    tok_s = world * wl.rows * args.steps / (ms / 1e3)
+    tok_s = job_tokens_per_s(world, wl.rows, args.steps, ms / 1e3)
 
     # ---- end to end through dec_step with host buffers ----
     host_recs = [(np.array(r[:wl.rows], np.int32), np.array(r[wl.rows:2 * wl.rows], np.int32),
@@ -236,11 +248,8 @@ def run_ours(args, rank, world, local_rank):
         t_, p_, w_ = host_recs[i % len(recs)]
         dec.step(t_, p_, w_, logits=False)
     e2e_s = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([e2e_s], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e_tok_s = world * wl.rows * args.steps / e2e_s
+    e2e_s = max_over_ranks(e2e_s, world, dev)
+    e2e_tok_s = job_tokens_per_s(world, wl.rows, args.steps, e2e_s)
 
     # ---- dominant kernel alone: RMSNorm + gate/up GEMV cycling the layers (graph
     # strategy), or the whole-step kernel (persistent strategy) ----
