@@ -31,8 +31,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "decode tokens/s and µs/token at 1 GB300; achieved HBM GB/s vs roofline"
 # committed ncu summaries: DRAM bytes per launch of the roofline kernel, valid while its source is unchanged
-PROFILES = {"persistent": (os.path.join(ROOT, "profiles", "persist_step_8b.md"), "persist.cu"),
-            "graph": (os.path.join(ROOT, "profiles", "gemv_gate_up_8b.md"), "gemv_impl.cuh")}
+# (the graph strategy has no full-size capture of its gate/up GEMV committed: its traffic stays null)
+PROFILES = {"persistent": (os.path.join(ROOT, "profiles", "persist_step_8b.md"), "persist.cu")}
 
 
 def _peaks():
@@ -112,6 +112,8 @@ class Clocks:
 def _traffic_from_profile(strategy):
     """DRAM bytes per launch of the roofline kernel from the committed ncu summary,
     or None if the summary is missing or the kernel source changed since."""
+    if strategy not in PROFILES:
+        return None
     path, src_name = PROFILES[strategy]
     try:
         txt = open(path).read()
@@ -153,6 +155,65 @@ def max_over_ranks(x: float, world: int, device="cpu") -> float:
 def job_tokens_per_s(world: int, rows: int, steps: int, seconds: float) -> float:
     """Whole-job throughput: every replica steps `rows` sequences `steps` times."""
     return world * rows * steps / seconds
+
+
+PHASES = ("qkv", "attn", "o", "gu", "down")
+
+
+def phase_bytes(wl) -> dict:
+    """Algorithmic bytes of each phase of one step: its weight matrix, or the
+    cap-swept K/V of one layer for attention."""
+    es = 2 if wl.wdtype == "bf16" else 4
+    kes = 2 if wl.kvdtype == "bf16" else 4
+    qd, kvd = wl.n_heads * wl.head_dim, wl.n_kv_heads * wl.head_dim
+    return {"qkv": (qd + 2 * kvd) * wl.d_model * es, "attn": wl.rows * 2 * wl.cap * kvd * kes,
+            "o": wl.d_model * qd * es, "gu": 2 * wl.ffn_hidden * wl.d_model * es,
+            "down": wl.d_model * wl.ffn_hidden * es, "head": wl.vocab * wl.d_model * es}
+
+
+def summarize_timeline(stamps, wl) -> dict:
+    """Per phase kind, from the in-kernel %globaltimer stamps of one step
+    (ns; row p = phase p: earliest CTA start, latest CTA past its wait, earliest
+    CTA end, latest CTA end): mean duration (latest end to latest end), the
+    rate of the phase's algorithmic bytes over it, the spread of CTA end times,
+    and the latency from the previous phase's latest end to the latest CTA
+    past this phase's wait."""
+    t = (np.asarray(stamps, dtype=np.float64) - float(stamps[0][0])) / 1e3
+    nb = phase_bytes(wl)
+    n_ph = t.shape[0]
+    acc = {}
+    for p in range(1, n_ph):
+        k = "head" if p == n_ph - 1 else PHASES[(p - 1) % 5]
+        a = acc.setdefault(k, [0, 0.0, 0.0, 0.0])
+        a[0] += 1
+        a[1] += t[p, 3] - t[p - 1, 3]
+        a[2] += t[p, 3] - t[p, 2]
+        a[3] += t[p, 1] - t[p - 1, 3]
+    out = {}
+    for k, (n, dur, spread, lat) in acc.items():
+        out[k] = {"phases": n, "us_mean": round(dur / n, 3), "gbs": round(nb[k] / (dur / n) / 1e3, 1),
+                  "end_spread_us": round(spread / n, 3), "wait_latency_us": round(lat / n, 3),
+                  "us_total": round(dur, 2)}
+    out["span_us"] = round(float(t[n_ph - 1, 3]), 2)
+    return out
+
+
+def phase_timeline(dec, dev_slots, n_rec, wl, reps=3) -> list:
+    """Traced replays (outside any timed region), one summary per slot record and repeat."""
+    from graph_replay_gb300 import _binding as B
+    n_ph = 5 * wl.n_layers + 2
+    res = []
+    for i in range(n_rec):
+        for _ in range(reps):
+            B.dec_trace(dec.h, True)
+            dec.launch(dev_slots[i])
+            dec.wait()
+            stamps = B.dec_trace_read(dec.h, n_ph)
+            B.dec_trace(dec.h, False)
+            s = summarize_timeline(stamps, wl)
+            s["record"] = i
+            res.append(s)
+    return res
 
 
 def run_ours(args, rank, world, local_rank):
@@ -301,6 +362,15 @@ def run_ours(args, rank, world, local_rank):
         "graph_launches_per_step": 1,
         "clocks": clk,
     }
+    if args.trace:
+        out["phase_timeline"] = phase_timeline(dec, dev_slots, len(recs), wl)
+        for s in out["phase_timeline"]:
+            print(f"record {s['record']} (pos {plist[s['record']]}): span {s['span_us']} us", file=sys.stderr)
+            for k in PHASES + ("head",):
+                v = s[k]
+                print(f"  {k:5s} x{v['phases']:<3d} {v['us_mean']:8.2f} us  {v['gbs']:7.1f} GB/s  "
+                      f"end spread {v['end_spread_us']:6.2f} us  wait latency {v['wait_latency_us']:5.2f} us",
+                      file=sys.stderr)
     if mw is not None and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(wl, mw, plist, toks, seconds=args.cpu_seconds)
     dec.close()
@@ -367,6 +437,9 @@ def main():
                     help="graph: the step's kernel sequence in one CUDA graph; persistent: one whole-step kernel")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (reduced case for profilers)")
     ap.add_argument("--vocab", type=int, default=0, help="override the vocabulary (reduced case for profilers)")
+    ap.add_argument("--trace", action="store_true",
+                    help="after the timed region, replay each slot record with the in-kernel phase trace on and "
+                         "report per-phase durations (stderr, and phase_timeline in the JSON line)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
