@@ -32,6 +32,8 @@ DEC_KV_CONTIGUOUS = 0
 DEC_KV_PAGED = 1
 DEC_STRATEGY_GRAPH = 0
 DEC_STRATEGY_PERSISTENT = 1
+DEC_SWEEP_CAP = 0
+DEC_SWEEP_POS = 1
 
 (DEC_W_EMBED, DEC_W_ATTN_NORM, DEC_W_Q, DEC_W_K, DEC_W_V, DEC_W_O, DEC_W_FFN_NORM, DEC_W_GATE, DEC_W_UP,
  DEC_W_DOWN, DEC_W_FINAL_NORM, DEC_W_LM_HEAD) = range(12)
@@ -80,6 +82,7 @@ _SIG = [
     ("dec_set_sampler", ctypes.c_int, [_P, _P]),
     ("dec_logprobs", ctypes.c_int, [_P, _I32, _P, _P]),
     ("dec_set_strategy", ctypes.c_int, [_P, _I32]),
+    ("dec_set_kv_sweep", ctypes.c_int, [_P, _I32]),
     ("dec_set_eager", ctypes.c_int, [_P, _I32]),
     ("dec_reset_state", ctypes.c_int, [_P]),
     ("dec_kv_ptr", ctypes.c_int, [_P, _I32, _I32, ctypes.POINTER(_P), ctypes.POINTER(ctypes.c_size_t)]),
@@ -222,6 +225,10 @@ def dec_prefill(h, pages_ptr, tokens_ptr, n: int, pos0: int, logits_ptr, id_ptr)
 
 def dec_set_strategy(h, strategy: int) -> None:
     check(h, lib().dec_set_strategy(h, strategy))
+
+
+def dec_set_kv_sweep(h, sweep: int) -> None:
+    check(h, lib().dec_set_kv_sweep(h, sweep))
 
 
 def dec_set_eager(h, eager: bool) -> None:

@@ -127,8 +127,9 @@ __global__ void __launch_bounds__(AM_THREADS, 2) k_attn_mma(const __grid_constan
         abort_s = 0;
         mbar_fence_init();
         // the first ring fill does not depend on the previous kernel -- unless
-        // that kernel wrote this step's keys (rows may share pages)
-        if (!p.kv_prewritten)
+        // that kernel wrote this step's keys (rows may share pages), or the
+        // fill is bounded by pos (read after the wait)
+        if (!p.kv_prewritten && !p.pos_bound)
             for (; issued < min(S, nst); ++issued) issue(issued);
         tr = trace_if_on(p.trace);   // after the copies: the enable word is a global load
         trace_mark(tr, p.trace_id, 0);
@@ -136,12 +137,16 @@ __global__ void __launch_bounds__(AM_THREADS, 2) k_attn_mma(const __grid_constan
     __syncthreads();
 
     pdl_wait();
-    if (tid == 0) {
-        for (; issued < min(S, nst); ++issued) issue(issued);
-        trace_mark(tr, p.trace_id, 1);
-    }
     int pos = p.pos[r];
     pos = min(max(pos, 0), p.cap - 1);   // an out-of-range pos was flagged by the embedding kernel
+    // stages this split loads: all of them, or (pos-bounded sweep) those up to
+    // the one holding pos; the stages left out hold no visible key, so no
+    // arithmetic would have touched them
+    const int nld = !p.pos_bound ? nst : (pos < j0 ? 0 : min(nst, (pos - j0) / PPS + 1));
+    if (tid == 0) {
+        for (; issued < min(S, nld); ++issued) issue(issued);
+        trace_mark(tr, p.trace_id, 1);
+    }
     const float* qrow = p.qkv + (size_t)r * p.qkv_stride;
     const float2* rt = p.rope + (size_t)pos * (HD / 2);
     for (int i = tid; i < G * (HD / 2); i += AM_THREADS) {
@@ -205,7 +210,7 @@ __global__ void __launch_bounds__(AM_THREADS, 2) k_attn_mma(const __grid_constan
 #pragma unroll
     for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
 
-    for (int t = 0; t < nst; ++t) {
+    for (int t = 0; t < nld; ++t) {
         const int slot = t % S;
         if (!*abort_v && !mbar_wait(&full_bar[slot], (t / S) & 1)) {
             *abort_v = 1;
@@ -317,7 +322,7 @@ __global__ void __launch_bounds__(AM_THREADS, 2) k_attn_mma(const __grid_constan
             }
         }
         __syncthreads();   // every warp is done with slot `slot`
-        if (tid == 0 && !*abort_v && issued < nst) {
+        if (tid == 0 && !*abort_v && issued < nld) {
             fence_proxy_async_smem();   // generic writes to the slot (pos row) before the async refill
             issue(issued++);
         }

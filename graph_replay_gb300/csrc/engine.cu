@@ -124,6 +124,7 @@ struct dec_handle {
     bool pdl = true;
     bool eager = false;
     int strategy = DEC_STRATEGY_GRAPH;
+    int kv_sweep = DEC_SWEEP_CAP;
     PersistPlan persist;
 
     // weights by role
@@ -704,8 +705,12 @@ int dec_capture(dec_handle* h, int32_t cap, int32_t rows, int32_t kv_layout, int
                 ap.prewrite = true;
                 ap.p.kv_prewritten = 1;
             }
+            ap.p.pos_bound = h->kv_sweep == DEC_SWEEP_POS ? 1 : 0;
             continue;
         }
+        if (h->kv_sweep == DEC_SWEEP_POS)
+            return fail(h, DEC_E_UNSUPPORTED,
+                        "DEC_SWEEP_POS needs the tensor-core attention kernel (bf16 K/V, head_dim 64 or 128)");
         if ((e = attn_plan(&ap, h->num_sms)) != cudaSuccess)
             return fail(h, DEC_E_UNSUPPORTED, "no attention kernel for head_dim=%d group=%d cap=%d (%s)", hd,
                         Hq / Hkv, cap, cudaGetErrorString(e));
@@ -715,6 +720,8 @@ int dec_capture(dec_handle* h, int32_t cap, int32_t rows, int32_t kv_layout, int
     if ((e = cudaMemsetAsync(h->d_trace, 0, sizeof(unsigned long long), h->stream)) != cudaSuccess)
         return cuda_fail(h, e, "trace clear");
     if (h->strategy == DEC_STRATEGY_PERSISTENT) {
+        if (h->kv_sweep == DEC_SWEEP_POS)
+            return fail(h, DEC_E_UNSUPPORTED, "DEC_SWEEP_POS is available with DEC_STRATEGY_GRAPH only");
         if (c.weight_dtype != DEC_DTYPE_BF16 || c.kv_dtype != DEC_DTYPE_BF16)
             return fail(h, DEC_E_UNSUPPORTED, "the persistent strategy needs bf16 weights and KV");
         PersistParams& pp = h->persist.p;
@@ -1045,6 +1052,15 @@ int dec_set_strategy(dec_handle* h, int32_t strategy) {
     if (strategy != DEC_STRATEGY_GRAPH && strategy != DEC_STRATEGY_PERSISTENT)
         return fail(h, DEC_E_INVALID, "unknown strategy %d", strategy);
     h->strategy = strategy;
+    return DEC_OK;
+}
+
+int dec_set_kv_sweep(dec_handle* h, int32_t sweep) {
+    int rc = gate(h, false);
+    if (rc) return rc;
+    if (h->captured) return fail(h, DEC_E_STATE, "the K/V sweep is chosen before dec_capture");
+    if (sweep != DEC_SWEEP_CAP && sweep != DEC_SWEEP_POS) return fail(h, DEC_E_INVALID, "unknown K/V sweep %d", sweep);
+    h->kv_sweep = sweep;
     return DEC_OK;
 }
 

@@ -103,6 +103,7 @@ struct AttnParams {
     float* out;            // [R, Hq * hd]
     unsigned* err;
     int kv_prewritten;     // 1: every row's new k, v are already in the store (k_kv_write ran)
+    int pos_bound;         // 1: a split loads no K/V tile after the one holding pos (DEC_SWEEP_POS)
     float scale;
     unsigned long long* trace;
     int trace_id;

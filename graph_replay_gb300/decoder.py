@@ -61,7 +61,8 @@ class Decoder:
 
     def __init__(self, cfg: B.dec_config, weights: dict, cap: int, rows: int = 1, kv_layout: str = "contiguous",
                  page_size: int = 16, num_pages: int = 0, stream: Optional[torch.cuda.Stream] = None,
-                 lib_workspace: bool = False, strategy: str = "graph", sampler: Optional[dict] = None):
+                 lib_workspace: bool = False, strategy: str = "graph", sampler: Optional[dict] = None,
+                 kv_sweep: str = "cap"):
         self.cfg = cfg
         self.rows, self.cap = rows, cap
         self.layout = B.DEC_KV_PAGED if kv_layout == "paged" else B.DEC_KV_CONTIGUOUS
@@ -72,6 +73,8 @@ class Decoder:
         try:
             B.dec_load_weights(self.h, self._bindings(weights))
             B.dec_set_strategy(self.h, B.DEC_STRATEGY_PERSISTENT if strategy == "persistent" else B.DEC_STRATEGY_GRAPH)
+            # "cap": the constant-shape sweep of [0, cap); "pos": stop at the tile holding pos (same results)
+            B.dec_set_kv_sweep(self.h, B.DEC_SWEEP_POS if kv_sweep == "pos" else B.DEC_SWEEP_CAP)
             if sampler is not None:   # records the sampling kernel after the head
                 B.check(self.h, B.dec_set_sampler(self.h, make_sampler(**sampler)))
             self.ws = None

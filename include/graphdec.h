@@ -95,6 +95,19 @@ typedef enum dec_kv_layout { DEC_KV_CONTIGUOUS = 0, DEC_KV_PAGED = 1 } dec_kv_la
  *               (DEC_E_UNSUPPORTED at capture otherwise). */
 typedef enum dec_strategy { DEC_STRATEGY_GRAPH = 0, DEC_STRATEGY_PERSISTENT = 1 } dec_strategy;
 
+/* Which K/V positions the attention of the captured step reads:
+ *   CAP  the method's constant-shape sweep of [0, cap) with the position mask
+ *        ("Execution", "A constant-shape decode graph": attention always
+ *        sweeps [cap]; a mask computed from Slot::Pos against an iota hides
+ *        the positions after pos) -- the default;
+ *   POS  the same captured graph and grid, but each split stops loading K/V
+ *        tiles after the one holding pos (a split that starts after pos loads
+ *        none).  The tiles it skips are fully masked, and the kernel already
+ *        does no arithmetic on a 16-key block without a visible key, so the
+ *        results are bit-identical to CAP; only the bytes read shrink from the
+ *        capacity to the positions up to pos. */
+typedef enum dec_kv_sweep { DEC_SWEEP_CAP = 0, DEC_SWEEP_POS = 1 } dec_kv_sweep;
+
 /* Model configuration.  RMSNorm is x / sqrt(mean(x^2) + rms_eps) * g; RoPE is
  * the half-split rotation of pairs (i, i + head_dim/2) by pos * rope_theta^(-2i/head_dim);
  * attention scale is 1/sqrt(head_dim); q head i reads kv head i / (n_heads / n_kv_heads). */
@@ -315,6 +328,13 @@ int dec_logprobs(dec_handle *h, int32_t n, int32_t *ids_out, float *logprobs_out
 /* Choose the execution strategy (dec_strategy) for the coming dec_capture;
  * DEC_E_STATE after capture.  Default DEC_STRATEGY_GRAPH. */
 int dec_set_strategy(dec_handle *h, int32_t strategy);
+
+/* Choose the K/V sweep (dec_kv_sweep) of the coming dec_capture; DEC_E_STATE
+ * after capture, DEC_E_INVALID for an unknown value.  Default DEC_SWEEP_CAP.
+ * DEC_SWEEP_POS needs the GRAPH strategy and the tensor-core attention kernel
+ * (bf16 K/V, head_dim 64 or 128): dec_capture returns DEC_E_UNSUPPORTED
+ * otherwise.  It also applies to dec_attention on the same handle. */
+int dec_set_kv_sweep(dec_handle *h, int32_t sweep);
 
 /* 1: later steps launch the recorded kernel sequence directly on the stream
  * instead of replaying the graph (same kernels, same arguments); 0: replay. */
