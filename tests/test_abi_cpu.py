@@ -97,3 +97,23 @@ def test_no_cpu_fallback_without_library(tmp_path):
     from graph_replay_gb300 import _binding as B
     with pytest.raises(ImportError):
         B.load_library(str(tmp_path / "missing.so"))
+
+
+def test_every_handle_call_refuses_a_null_handle(lib):
+    # no device is touched: the handle check comes first in every entry point
+    import ctypes as C
+    from graph_replay_gb300 import _binding as B
+    skip = {"dec_init", "dec_workspace_size", "dec_last_error", "dec_status_str"}
+    checked = 0
+    for name, _, argtypes in B._SIG:
+        if name in skip:
+            continue
+        args = []
+        for t in argtypes:
+            if t in (C.c_int32, C.c_int64, C.c_size_t, C.c_int):
+                args.append(1)
+            else:
+                args.append(None)
+        assert getattr(lib, name)(*args) == B.DEC_E_INVALID, name
+        checked += 1
+    assert checked == len(B.SYMBOLS) - len(skip)
