@@ -117,3 +117,15 @@ def test_every_handle_call_refuses_a_null_handle(lib):
         assert getattr(lib, name)(*args) == B.DEC_E_INVALID, name
         checked += 1
     assert checked == len(B.SYMBOLS) - len(skip)
+
+
+def test_header_is_plain_c():
+    # the boundary is a C ABI: the header compiles as C99 (no C++ or torch types)
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler on this machine")
+    r = subprocess.run([cc, "-fsyntax-only", "-x", "c", "-std=c99", "-Wall", "-Wextra", "-Werror", HEADER],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
