@@ -3,6 +3,10 @@
 TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
 benchmark's ``cpu_baseline`` leg are the only callers.  Nothing in the
 ``graph_replay_gb300`` package imports it, and it imports nothing from there.
+
+``ORACLE_LIB_UNDER_TEST`` (environment): load that compiled copy of
+``oracle.c`` instead of building this one.  Only the mutation test sets it, to
+check that the pins reject deliberately broken copies of the oracle.
 """
 from __future__ import annotations
 
@@ -50,7 +54,7 @@ def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
+            lib = ctypes.CDLL(os.environ.get("ORACLE_LIB_UNDER_TEST") or build())
             P, I, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_double
             I64 = ctypes.c_int64
             lib.orc_bf16_value.restype = D
