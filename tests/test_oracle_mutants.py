@@ -89,3 +89,52 @@ def test_pins_reject_every_planted_slip(workdir):
     assert not missed, f"slips no pin caught by failing: {missed}"
     for name, (_, pin) in sorted(results.items()):
         print(f"{name}: caught by {pin}")
+
+
+# slips in the sampling suffix's oracle (Python): (slip, function, text, replacement)
+PY_MUTANTS = [
+    ("top-p cut takes the prefix before reaching top_p", "sample", "S >= min(top_p, 1.0) * S[-1]",
+     "S > min(top_p, 1.0) * S[-1]"),
+    ("min-p relative to the total instead of the largest", "sample", "np.count_nonzero(q >= min_p)",
+     "np.count_nonzero(q / S[-1] >= min_p)"),
+    ("temperature multiplies", "sample", "(l[order] - l[order[0]]) / temperature",
+     "(l[order] - l[order[0]]) * temperature"),
+    ("ties go to the higher index", "sample", "np.lexsort((np.arange(l.size), -l))",
+     "np.lexsort((-np.arange(l.size), -l))"),
+    ("uniform from 52 bits", "uniform", ">> 11) * 2.0 ** -53", ">> 12) * 2.0 ** -53"),
+    ("splitmix64 increment", "splitmix64_at", "(counter + 1) * 0x9E3779B97F4A7C15", "counter * 0x9E3779B97F4A7C15"),
+    ("log-sum-exp loses the shift", "top_logprobs", "lse = m + np.log(", "lse = np.log("),
+]
+
+_PY_RUNNER = """
+import inspect, sys
+sys.path.insert(0, {root!r})
+import pytest
+import oracle
+src = inspect.getsource(getattr(oracle, {fn!r}))
+assert src.count({old!r}) == 1, "the text to mutate must occur once"
+ns = {{}}
+exec(src.replace({old!r}, {new!r}), oracle.__dict__, ns)
+setattr(oracle, {fn!r}, ns[{fn!r}])
+sys.exit(pytest.main([{pins!r}, "-x", "-q", "-rf", "-p", "no:cacheprovider"]))
+"""
+
+
+def _run_pins_patched(fn: str, old: str, new: str):
+    code = _PY_RUNNER.format(root=ROOT, fn=fn, old=old, new=new, pins=PINS)
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=600,
+                       env=dict(os.environ, OMP_NUM_THREADS="1"))
+    failed = [l.split("::", 1)[1].split(" ")[0] for l in r.stdout.splitlines() if l.startswith("FAILED ")]
+    return r.returncode, (failed[0] if failed else None), r.stdout + r.stderr
+
+
+def test_pins_reject_every_planted_sampling_slip():
+    # control: the same patching path with an identity replacement passes
+    rc, _, log = _run_pins_patched("sample", "S = np.cumsum(q)", "S = np.cumsum(q)")
+    assert rc == 0, log[-2000:]
+    with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
+        results = list(ex.map(lambda m: (m[0],) + _run_pins_patched(*m[1:]), PY_MUTANTS))
+    missed = {name: (rc, log[-400:]) for name, rc, pin, log in results if rc != 1 or pin is None}
+    assert not missed, f"slips no pin caught by failing: {missed}"
+    for name, _, pin, _ in results:
+        print(f"{name}: caught by {pin}")
