@@ -416,6 +416,17 @@ def run_reference(args):
     budget = max(5.0, min(120.0, args.cpu_seconds))
     cpu_baseline(wl, mw, plist, toks, seconds=0.0, steps_cap=max(1, min(args.warmup, 2)))
     cb = cpu_baseline(wl, mw, plist, toks, seconds=budget, steps_cap=args.steps)
+    # the same oracle on one thread: one decode step (one per row), reported beside the line
+    import oracle
+    try:
+        if oracle.set_threads(1) != 1:
+            raise RuntimeError("the oracle did not switch to one thread")
+        one = cpu_baseline(wl, mw, plist, toks, seconds=0.0, steps_cap=1)
+        cb["single_thread"] = {"value": one["value"], "unit": one["unit"], "cores": 1, "sample": one["sample"]}
+    except Exception as e:   # reported, never fatal: the line's value is the multi-core sample
+        cb["single_thread"] = {"unavailable": str(e)[:200]}
+    finally:
+        oracle.set_threads(cb["cores"])
     return {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "tokens/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",

@@ -77,6 +77,10 @@ def _load():
             lib.orc_argmax.argtypes = [P, I]
             lib.orc_step.restype = I
             lib.orc_step.argtypes = [ctypes.POINTER(OrcModel), P, P, I, I, I, P, P]
+            lib.orc_set_threads.restype = None
+            lib.orc_set_threads.argtypes = [I]
+            lib.orc_threads.restype = I
+            lib.orc_threads.argtypes = []
             lib.orc_full_causal.restype = I
             lib.orc_full_causal.argtypes = [ctypes.POINTER(OrcModel), P, I, P, P, P]
             _lib = lib
@@ -157,6 +161,14 @@ def attend(q, K, V) -> np.ndarray:
 def argmax(v) -> int:
     v = _f64(v)
     return _load().orc_argmax(v.ctypes.data, v.size)
+
+
+def set_threads(n: int) -> int:
+    """Thread count of the oracle's parallel loops (for timing; results do not
+    depend on it).  Returns the count now in effect."""
+    lib = _load()
+    lib.orc_set_threads(int(n))
+    return lib.orc_threads()
 
 
 def top2_margin(logits) -> float:

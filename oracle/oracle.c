@@ -171,6 +171,13 @@ void orc_attend(const double *q, const void *K, const void *V, int kvdt, int64_t
     free(a);
 }
 
+/* threads of the parallel loops over output rows and heads (timing only: the
+   results do not depend on it) */
+extern void omp_set_num_threads(int);   /* OpenMP runtime API (linked with -fopenmp) */
+extern int omp_get_max_threads(void);
+void orc_set_threads(int n) { omp_set_num_threads(n > 0 ? n : 1); }
+int orc_threads(void) { return omp_get_max_threads(); }
+
 /* index of the largest value, lowest index on ties */
 int orc_argmax(const double *v, int n) {
     int best = 0;

@@ -35,6 +35,8 @@ def test_reference_arm_prints_the_contract_line():
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
     assert d["config"]["workload"].startswith("tiny:")
+    st = cb["single_thread"]
+    assert st["cores"] == 1 and st["value"] > 0 and st["unit"] == "tokens/s"
 
 
 def test_reference_arm_other_ranks_exit_quietly():
