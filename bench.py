@@ -371,10 +371,46 @@ def run_ours(args, rank, world, local_rank):
                 print(f"  {k:5s} x{v['phases']:<3d} {v['us_mean']:8.2f} us  {v['gbs']:7.1f} GB/s  "
                       f"end spread {v['end_spread_us']:6.2f} us  wait latency {v['wait_latency_us']:5.2f} us",
                       file=sys.stderr)
+    dec.close()
+    if persistent and world == 1 and not args.no_graph_leg:
+        out["graph_strategy"] = graph_strategy_leg(args, wl, cfg, w, slot_map, dev_slots, hbm_peak)
     if mw is not None and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(wl, mw, plist, toks, seconds=args.cpu_seconds)
-    dec.close()
     return out
+
+
+def graph_strategy_leg(args, wl, cfg, w, slot_map, dev_slots, hbm_peak) -> dict:
+    """The pages' own strategy on the same workload, timed after the main line:
+    the step's kernel sequence (embedding, 5 fused kernels per layer, head)
+    recorded into one CUDA graph, one graph launch per step, same weights,
+    slot records and timing method (CUDA events on the handle's stream)."""
+    import torch
+    from graph_replay_gb300 import Decoder
+    dec = Decoder(cfg, w, cap=wl.cap, rows=wl.rows, kv_layout=wl.layout, page_size=wl.page_size,
+                  num_pages=wl.num_pages, strategy="graph")
+    if slot_map is not None:
+        dec.set_slot_map(slot_map)
+    n = len(dev_slots)
+    steps = max(1, min(args.steps, 200))
+    for i in range(args.warmup):
+        dec.launch(dev_slots[i % n])
+    torch.cuda.synchronize()
+    stream = dec.stream()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        dec.launch(dev_slots[i % n])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    dec.wait()
+    ms = e0.elapsed_time(e1) / steps
+    kernels = dec.stats()["kernels_per_step"]
+    dec.close()
+    gbs = wl.step_bytes() / (ms * 1e-3) / 1e9
+    return {"ms_per_step": round(ms, 5), "tokens_per_s": round(wl.rows / (ms * 1e-3), 3), "steps": steps,
+            "kernels_per_step": kernels, "achieved_gbs": round(gbs, 1), "frac": round(gbs / hbm_peak, 4),
+            "frac_of_8tbs": round(gbs / 8000.0, 4)}
 
 
 def cpu_baseline(wl, mw, plist, toks, seconds=20.0, steps_cap=None):
@@ -444,6 +480,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph-leg", action="store_true",
+                    help="skip timing the multi-kernel graph strategy beside the persistent line")
     ap.add_argument("--strategy", default="persistent", choices=["graph", "persistent"],
                     help="graph: the step's kernel sequence in one CUDA graph; persistent: one whole-step kernel")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (reduced case for profilers)")

@@ -25,6 +25,7 @@ DEC_FAULT_TOKEN = 0x1
 DEC_FAULT_POS = 0x2
 DEC_FAULT_WRITE_MAP = 0x4
 DEC_FAULT_SLOT_MAP = 0x8
+DEC_FAULT_WAIT = 0x10
 
 DEC_DTYPE_F32 = 0
 DEC_DTYPE_BF16 = 1
@@ -91,11 +92,13 @@ _SIG = [
     ("dec_logits_ptr", ctypes.c_int, [_P, ctypes.POINTER(_P)]),
     ("dec_stream", ctypes.c_int, [_P, ctypes.POINTER(_P)]),
     ("dec_stats_get", ctypes.c_int, [_P, ctypes.POINTER(dec_stats)]),
+    ("dec_slot_map_ptr", ctypes.c_int, [_P, ctypes.POINTER(_P)]),
     ("dec_launch_kernel", ctypes.c_int, [_P, _I32, _I32, ctypes.POINTER(_I64)]),
     ("dec_trace", ctypes.c_int, [_P, _I32]),
     ("dec_trace_read", ctypes.c_int, [_P, _P, ctypes.c_size_t]),
     ("dec_debug_busy", ctypes.c_int, [_P, _I64]),
     ("dec_set_timeout", ctypes.c_int, [_P, _I64]),
+    ("dec_debug_wait", ctypes.c_int, [_P, ctypes.c_uint32, ctypes.c_uint32, _I32, _I32]),
     ("dec_last_error", ctypes.c_char_p, [_P]),
     ("dec_status_str", ctypes.c_char_p, [ctypes.c_int]),
     ("dec_destroy", ctypes.c_int, [_P]),
@@ -272,6 +275,12 @@ def dec_stats_get(h) -> dec_stats:
     return st
 
 
+def dec_slot_map_ptr(h) -> int:
+    p = ctypes.c_void_p()
+    check(h, lib().dec_slot_map_ptr(h, ctypes.byref(p)))
+    return p.value
+
+
 def dec_launch_kernel(h, index: int, pdl: bool = False) -> int:
     n = ctypes.c_int64()
     check(h, lib().dec_launch_kernel(h, index, 1 if pdl else 0, ctypes.byref(n)))
@@ -295,6 +304,10 @@ def dec_debug_busy(h, microseconds: int) -> None:
 
 def dec_set_timeout(h, ms: int) -> None:
     check(h, lib().dec_set_timeout(h, ms))
+
+
+def dec_debug_wait(h, grid_polls: int = 0, ring_polls: int = 0, hold_phase: int = -1, drop_stage: int = -1) -> None:
+    check(h, lib().dec_debug_wait(h, grid_polls, ring_polls, hold_phase, drop_stage))
 
 
 def dec_destroy(h) -> int:

@@ -57,8 +57,8 @@ int es_of(int dtype) { return dtype == DEC_DTYPE_BF16 ? 2 : 4; }
 
 // Offsets of every buffer of a capture inside one workspace.
 struct WsLayout {
-    size_t status, slots, slot_map, counters, trace, ptabs, tmaps, gbar, x, qkv, attn, gu, logits, part, gpart, gcnt,
-        chain, sampler, rope, kv, kv_layer, total;
+    size_t status, slots, slot_map, counters, trace, ptabs, tmaps, gbar, dbg, x, qkv, attn, gu, logits, part, gpart,
+        gcnt, chain, sampler, rope, kv, kv_layer, total;
 };
 
 // kernels recorded per step: embedding, 5 per layer, head
@@ -79,6 +79,7 @@ bool compute_layout(const dec_config& c, int cap, int R, int layout, int page, i
     L->ptabs = take((size_t)c.n_layers * 11 * sizeof(void*));
     L->tmaps = take(persist_tmap_bytes(c.n_layers));
     L->gbar = take(((size_t)kernels_per_step(c.n_layers) + 2) * sizeof(unsigned));
+    L->dbg = take(4 * sizeof(unsigned));   // persistent kernel: wait bounds and test hooks (zero: defaults)
     L->x = take((size_t)R * d * 4);
     L->qkv = take((size_t)R * (Hq + 2 * Hkv) * hd * 4);
     L->attn = take((size_t)R * Hq * hd * 4);
@@ -226,6 +227,15 @@ int bounded_wait(dec_handle* h) {
             if (ms > 2.0) std::this_thread::sleep_for(std::chrono::microseconds(20));
         }
     }
+}
+
+// Host -> device copy ordered on the handle's stream, waited for (bounded): the
+// source may change as soon as this returns, and the handle's non-blocking
+// stream does not order itself after a legacy-stream cudaMemcpy.
+int h2d_wait(dec_handle* h, void* dst, const void* src, size_t bytes, const char* what) {
+    cudaError_t e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, h->stream);
+    if (e != cudaSuccess) return cuda_fail(h, e, what);
+    return bounded_wait(h);
 }
 
 int validate_config(const dec_config* c, dec_handle* h) {
@@ -417,8 +427,6 @@ int dec_init(const dec_config* cfg, dec_handle** out) {
     h->cfg = *cfg;
     if (h->cfg.wait_timeout_ms <= 0) h->cfg.wait_timeout_ms = 600000;
     h->lw.assign(cfg->n_layers, std::array<const void*, 9>{});
-    const char* env = getenv("GRAPHDEC_PDL");
-    h->pdl = !(env && env[0] == '0');
     cudaError_t e = cudaSetDevice(cfg->device);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, cfg->device);
     if (e != cudaSuccess) {
@@ -566,14 +574,14 @@ int dec_capture(dec_handle* h, int32_t cap, int32_t rows, int32_t kv_layout, int
     // RoPE table and the default page table (row r owns pages r*ppr .. r*ppr+ppr-1)
     {
         std::vector<float2> t = rope_table(cap, c.head_dim, c.rope_theta);
-        if ((e = cudaMemcpy(h->d_rope, t.data(), t.size() * sizeof(float2), cudaMemcpyHostToDevice)) != cudaSuccess)
-            return cuda_fail(h, e, "RoPE table upload");
+        if ((rc = h2d_wait(h, h->d_rope, t.data(), t.size() * sizeof(float2), "RoPE table upload")) != DEC_OK)
+            return rc;
         if (kv_layout == DEC_KV_PAGED) {
             h->slot_map_host.resize((size_t)rows * h->ppr);
             for (size_t i = 0; i < h->slot_map_host.size(); ++i) h->slot_map_host[i] = (int32_t)i;
-            e = cudaMemcpy(h->d_slot_map, h->slot_map_host.data(), h->slot_map_host.size() * sizeof(int32_t),
-                           cudaMemcpyHostToDevice);
-            if (e != cudaSuccess) return cuda_fail(h, e, "slot map upload");
+            if ((rc = h2d_wait(h, h->d_slot_map, h->slot_map_host.data(), h->slot_map_host.size() * sizeof(int32_t),
+                               "slot map upload")) != DEC_OK)
+                return rc;
         }
     }
 
@@ -740,6 +748,9 @@ int dec_capture(dec_handle* h, int32_t cap, int32_t rows, int32_t kv_layout, int
         pp.rope = h->d_rope; pp.tmaps = h->ws + L.tmaps;
         pp.err = &h->d_status->err; pp.amax = h->d_status->amax; pp.nonfinite = h->d_status->nonfinite;
         pp.bar = (unsigned*)(h->ws + L.gbar); pp.trace = h->d_trace;
+        pp.dbg = (const unsigned*)(h->ws + L.dbg);
+        if ((e = cudaMemsetAsync(h->ws + L.dbg, 0, 4 * sizeof(unsigned), h->stream)) != cudaSuccess)
+            return cuda_fail(h, e, "wait bound clear");
         if ((e = persist_plan(&h->persist, h->num_sms)) != cudaSuccess)
             return fail(h, DEC_E_UNSUPPORTED, "no persistent step kernel for this shape (%s)", cudaGetErrorString(e));
         std::vector<const void*> host_tab((size_t)c.n_layers * 11);
@@ -748,9 +759,9 @@ int dec_capture(dec_handle* h, int32_t cap, int32_t rows, int32_t kv_layout, int
             host_tab[9 * (size_t)c.n_layers + 2 * l] = h->K[l];
             host_tab[9 * (size_t)c.n_layers + 2 * l + 1] = h->V[l];
         }
-        if ((e = cudaMemcpy(ptab, host_tab.data(), host_tab.size() * sizeof(void*), cudaMemcpyHostToDevice)) !=
-            cudaSuccess)
-            return cuda_fail(h, e, "persistent table upload");
+        if ((rc = h2d_wait(h, ptab, host_tab.data(), host_tab.size() * sizeof(void*), "persistent table upload")) !=
+            DEC_OK)
+            return rc;
         std::vector<unsigned char> tm(persist_tmap_bytes(c.n_layers));
         std::vector<void*> kvp(2 * (size_t)c.n_layers);
         for (int l = 0; l < c.n_layers; ++l) {
@@ -759,14 +770,12 @@ int dec_capture(dec_handle* h, int32_t cap, int32_t rows, int32_t kv_layout, int
         }
         if ((e = persist_tmaps(pp, kvp.data(), tm.data())) != cudaSuccess)
             return fail(h, DEC_E_UNSUPPORTED, "tensor maps for the persistent kernel (%s)", cudaGetErrorString(e));
-        if ((e = cudaMemcpy(h->ws + L.tmaps, tm.data(), tm.size(), cudaMemcpyHostToDevice)) != cudaSuccess)
-            return cuda_fail(h, e, "tensor map upload");
+        if ((rc = h2d_wait(h, h->ws + L.tmaps, tm.data(), tm.size(), "tensor map upload")) != DEC_OK) return rc;
     }
 
     // the sampler's parameter slot (read by the recorded sampling kernel)
-    if (h->sampler_on &&
-        (e = cudaMemcpy(h->ws + L.sampler, &h->sampler, sizeof(SamplerSlot), cudaMemcpyHostToDevice)) != cudaSuccess)
-        return cuda_fail(h, e, "sampler upload");
+    if (h->sampler_on && (rc = h2d_wait(h, h->ws + L.sampler, &h->sampler, sizeof(SamplerSlot), "sampler upload")) != DEC_OK)
+        return rc;
 
     // ---- one eager step (launch checks), then a clean state ----
     if ((e = zero_state(h)) != cudaSuccess) return cuda_fail(h, e, "state clear");
@@ -811,9 +820,7 @@ int dec_set_slot_map(dec_handle* h, const int32_t* map) {
     // wait for in-flight steps before rewriting the slot buffer
     if ((rc = bounded_wait(h)) != DEC_OK) return rc;
     h->slot_map_host.assign(map, map + n);
-    cudaError_t e = cudaMemcpy(h->d_slot_map, map, n * sizeof(int32_t), cudaMemcpyHostToDevice);
-    if (e != cudaSuccess) return cuda_fail(h, e, "slot map upload");
-    return DEC_OK;
+    return h2d_wait(h, h->d_slot_map, h->slot_map_host.data(), n * sizeof(int32_t), "slot map upload");
 }
 
 int dec_step(dec_handle* h, const int32_t* tokens, const int32_t* pos, const int32_t* write_map, float* logits_out,
@@ -1139,6 +1146,27 @@ int dec_stats_get(const dec_handle* h, dec_stats* out) {
     return DEC_OK;
 }
 
+int dec_slot_map_ptr(dec_handle* h, int32_t** ptr) {
+    int rc = gate(h, true);
+    if (rc) return rc;
+    if (h->layout != DEC_KV_PAGED) return fail(h, DEC_E_STATE, "the capture uses contiguous KV");
+    if (!ptr) return fail(h, DEC_E_INVALID, "ptr is NULL");
+    *ptr = h->d_slot_map;
+    return DEC_OK;
+}
+
+int dec_debug_wait(dec_handle* h, uint32_t grid_polls, uint32_t ring_polls, int32_t hold_phase, int32_t drop_stage) {
+    int rc = gate(h, true);
+    if (rc) return rc;
+    if (h->strategy != DEC_STRATEGY_PERSISTENT)
+        return fail(h, DEC_E_STATE, "the wait hooks belong to the persistent strategy");
+    if (hold_phase < -1 || drop_stage < -1) return fail(h, DEC_E_INVALID, "hold_phase and drop_stage must be >= -1");
+    // the kernel reads the block at its start: write it between launches
+    if ((rc = bounded_wait(h)) != DEC_OK) return rc;
+    const unsigned v[4] = {grid_polls, ring_polls, (unsigned)(hold_phase + 1), (unsigned)(drop_stage + 1)};
+    return h2d_wait(h, h->ws + h->lay.dbg, v, sizeof v, "wait bound write");
+}
+
 int dec_launch_kernel(dec_handle* h, int32_t index, int32_t pdl, int64_t* bytes) {
     int rc = gate(h, true);
     if (rc) return rc;
@@ -1203,9 +1231,7 @@ int dec_trace(dec_handle* h, int32_t enable) {
         init[1 + 4 * k + 0] = ~0ull;   // minima start high
         init[1 + 4 * k + 2] = ~0ull;
     }
-    cudaError_t e = cudaMemcpy(h->d_trace, init.data(), n * sizeof(unsigned long long), cudaMemcpyHostToDevice);
-    if (e != cudaSuccess) return cuda_fail(h, e, "trace reset");
-    return DEC_OK;
+    return h2d_wait(h, h->d_trace, init.data(), n * sizeof(unsigned long long), "trace reset");
 }
 
 int dec_trace_read(dec_handle* h, uint64_t* out, size_t n_kernels) {
@@ -1213,9 +1239,10 @@ int dec_trace_read(dec_handle* h, uint64_t* out, size_t n_kernels) {
     if (rc) return rc;
     if (!out || n_kernels > (size_t)h->kernels) return fail(h, DEC_E_INVALID, "dec_trace_read: bad buffer");
     if ((rc = bounded_wait(h)) != DEC_OK) return rc;
-    cudaError_t e = cudaMemcpy(out, h->d_trace + 1, 4 * n_kernels * sizeof(unsigned long long), cudaMemcpyDeviceToHost);
+    cudaError_t e = cudaMemcpyAsync(out, h->d_trace + 1, 4 * n_kernels * sizeof(unsigned long long),
+                                    cudaMemcpyDeviceToHost, h->stream);
     if (e != cudaSuccess) return cuda_fail(h, e, "trace read");
-    return DEC_OK;
+    return bounded_wait(h);
 }
 
 }  // extern "C"
@@ -1260,7 +1287,10 @@ void engine_attention_scratch(const dec_handle* h, size_t* part_floats, size_t* 
 }
 
 int engine_gate(dec_handle* h) { return gate(h, true); }
-int engine_fail(dec_handle* h, int code, const char* msg) { return fail(h, code, "%s", msg); }
+int engine_fail(dec_handle* h, int code, const char* msg) {
+    if (code == DEC_E_CUDA) h->state = ST_POISONED;   // CUDA errors are sticky, as everywhere in the ABI
+    return fail(h, code, "%s", msg);
+}
 int engine_device(const dec_handle* h) { return h->cfg.device; }
 
 }  // namespace gd

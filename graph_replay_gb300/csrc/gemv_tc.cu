@@ -464,13 +464,6 @@ const void* gemv_tc_kernel(int pro, int epi, int ws) {
 }
 
 namespace {
-int act_budget() {
-    if (const char* env = getenv("GRAPHDEC_TC_ACT_KB")) {   // resident activation budget (tuning)
-        const long v = atol(env);
-        if (v >= 32 && v <= 160) return (int)v * 1024;
-    }
-    return TC_ACT_BUDGET_DEFAULT;
-}
 // K splits: the fewest whose K range is a multiple of the stage width
 // (>= 1024 columns) and whose activations fit the budget; 0 if none
 int tc_splits(int R, int K, int budget) {
@@ -485,17 +478,10 @@ int tc_splits(int R, int K, int budget) {
 }  // namespace
 
 size_t gemv_tc_part_floats(int R, int K, int N, bool paired) {
-    // the largest need over the budgets the plan may use
-    size_t most = 0;
-    for (int budget : {32 * 1024, 64 * 1024, 96 * 1024, 128 * 1024, 160 * 1024, act_budget()}) {
-        const int ks = tc_splits(R, K, budget);
-        if (ks > 1) {
-            const size_t need = (size_t)ks * R * (size_t)N + (size_t)ks * GEMV_TC_CNT_WORDS * 8;
-            if (need > most) most = need;
-        }
-    }
+    // the need at the plan's resident activation budget
+    const int ks = tc_splits(R, K, TC_ACT_BUDGET_DEFAULT);
     (void)paired;   // N already counts both halves of a gate/up pair
-    return most;
+    return ks > 1 ? (size_t)ks * R * (size_t)N + (size_t)ks * GEMV_TC_CNT_WORDS * 8 : 0;
 }
 
 cudaError_t gemv_tc_plan(GemvPlan* plan, int num_sms) {
@@ -512,7 +498,7 @@ cudaError_t gemv_tc_plan(GemvPlan* plan, int num_sms) {
         return cudaErrorInvalidValue;
     const void* fn = gemv_tc_kernel(plan->pro, plan->epi, TC_WS_MAX);
     if (!fn) return cudaErrorInvalidValue;
-    const int ks = tc_splits(p.R, p.K, act_budget());
+    const int ks = tc_splits(p.R, p.K, TC_ACT_BUDGET_DEFAULT);
     if (ks < 1) return cudaErrorInvalidValue;
     const int kq = p.K / ks;
     int dev = 0, optin = 0;

@@ -224,7 +224,9 @@ struct PersistParams {
     unsigned long long* trace;
     int split_len, nsplit;
     int rps_d, rps_f;          // weight rows per ring stage for K = d and K = F
-    int pf;                    // stages beyond the ring's reach prefetched into L2 by the producer
+    const unsigned* dbg;       // [4] wait bounds and test hooks: grid-wait polls, ring-wait polls (0: defaults),
+                               // phase whose grid-wait target is raised by one + 1, stage CTA 0 never issues + 1
+                               // (0: none); 16-byte aligned
 };
 
 struct PersistPlan {

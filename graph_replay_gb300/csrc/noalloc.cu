@@ -3,24 +3,27 @@
 // caller or the library allocates.
 //
 // Why: some callers cannot allocate device memory at the point where they run
-// attention -- code executing inside a stream capture that must not add
-// allocation nodes, host callbacks (which may not call CUDA at all beyond
-// stream-ordered work), or serving loops with a fixed device-memory budget
-// where cudaMalloc/cudaFree would synchronise the device or fail.  This entry
-// point performs no allocation of any kind: the split partials and the
-// completion counters live in one file-scope __device__ array of a fixed size.
+// attention.  A serving process that sized its weights and KV cache to fill
+// the GPU up front has no memory left to hand out per call, and a latency-bound
+// loop cannot absorb cudaMalloc / cudaFree, which may synchronise the whole
+// device.  This entry point performs no allocation of any kind: the split
+// partials and the completion counters live in one file-scope __device__ array
+// of a fixed size.  Like dec_attention it runs on the handle's stream and
+// waits (bounded) for its result.
 //
 // Costs and rules for a user:
-//   * every GPU that loads this library reserves the array (about 2 MiB) for
-//     as long as the library stays loaded;
+//   * every GPU that loads this library reserves the array (about 2 MiB) until
+//     the process exits;
 //   * all calls on a device share the array and it keeps the contents of the
 //     last call: the counters are cleared at the start of every call, and two
 //     calls whose work overlaps on the GPU (different streams, or several host
 //     threads) race on it -- serialise them;
 //   * the first call on each device resolves the array's device address
-//     (cudaGetSymbolAddress, with that device current); make that first call
-//     before any stream capture that includes this entry point;
-//   * shapes whose partials exceed the array are refused with DEC_E_UNSUPPORTED.
+//     (cudaGetSymbolAddress, with that device current) and keeps it for the
+//     life of the process; make that first call before any stream capture.  A
+//     cudaDeviceReset invalidates the address together with every handle;
+//   * shapes whose partials exceed the array are refused with
+//     DEC_E_UNSUPPORTED, and the handle stays usable.
 #include <mutex>
 
 #include "graphdec.h"
@@ -65,7 +68,7 @@ extern "C" int dec_attention_static(dec_handle* h, int32_t layer, const float* q
     size_t need_part = 0, need_ctr = 0;
     gd::engine_attention_scratch(h, &need_part, &need_ctr);
     if (need_part > STATIC_PART_FLOATS || need_ctr > STATIC_COUNTERS)
-        return gd::engine_fail(h, DEC_E_UNSUPPORTED,
+        return gd::engine_fail(h, DEC_E_UNSUPPORTED,   // refused before any device work: the handle stays usable
                                "dec_attention_static: this shape needs more split scratch than the fixed "
                                "2 MiB array holds (rows * n_heads * splits * (head_dim + 4) floats)");
     float* base = nullptr;

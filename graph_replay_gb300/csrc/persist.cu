@@ -3,28 +3,30 @@
 // The pages' own strategy records the step's dispatch sequence and replays it
 // ("Execution", "A constant-shape decode graph"; "Backends", "PTX (NVIDIA)");
 // they name a megakernel as a possible future strategy ("Architecture
-// Overview", "Current state").  This file is that alternative, built for
-// comparison: one cooperative kernel (one CTA per SM) runs every phase of the
-// step -- embedding; per layer RMSNorm+QKV, attention, O-proj, RMSNorm+gate/up,
-// SwiGLU+down; final norm + head + argmax -- and is captured as the graph's
-// single node, replayed per token exactly like the multi-kernel graph.
+// Overview", "Current state").  This file is that alternative: one cooperative
+// kernel (one CTA per SM) runs every phase of the step -- embedding; per layer
+// RMSNorm+QKV, attention, O-proj, RMSNorm+gate/up+SwiGLU, down; final norm +
+// head + argmax -- and is captured as the graph's single node, replayed per
+// token exactly like the multi-kernel graph.
 //
 // Why it is faster on this GPU: a phase moves 32-235 MB, so each kernel
 // boundary of the multi-kernel graph costs a ramp-up and a tail of several
-// microseconds with HBM partly idle.  Here thread 0 of each CTA streams the
-// CTA's whole step -- every phase's weight rows and K/V tiles, in phase order
-// -- through one ring of shared-memory stages (64 KB, bulk and TMA-tensor
-// copies).  The data of the next phase is already landing while the CTA waits
-// for the phase's grid-wide dependency, so the memory stream never stops.
+// microseconds with HBM partly idle.  Here a producer warp of each CTA (one
+// lane) streams the CTA's whole step -- every phase's weight rows and K/V
+// tiles, in phase order -- through one ring of shared-memory stages (64 KB,
+// bulk and TMA-tensor copies), while eight compute warps consume it.  The data
+// of the next phase is already landing while the compute warps wait for the
+// phase's grid-wide dependency, so the memory stream never stops.
 //
 // Phase dependencies are grid-wide counters: a CTA adds 1 to its phase's
-// counter after writing the phase's outputs (release fence), and waits until
-// a phase's counter reaches the grid size before reading that phase's outputs
-// (acquire load, bounded poll).  Data written by other CTAs is read through
-// L2 (ld.global.cg).  The cooperative launch guarantees that every CTA is
-// resident, so the waits always end; every wait is still bounded and sets
-// FAULT_WAIT (plus a grid-wide abort word) if it gives up.  The last CTA to
-// finish resets the counters for the next replay.
+// counter after writing the phase's outputs (release reduction), and waits
+// until a phase's counter reaches the grid size before reading that phase's
+// outputs (acquire load, bounded poll).  Data written by other CTAs is read
+// through L2 (ld.global.cg).  The cooperative launch guarantees that every CTA
+// is resident, so the waits always end; every wait is still bounded and sets
+// FAULT_WAIT (plus a grid-wide abort word) if it gives up, after which every
+// other wait returns at once.  The last CTA to finish resets the counters for
+// the next replay.
 //
 // The arithmetic of each phase is the multi-kernel graph's (gemv_impl.cuh and
 // attn_mma.cu): fixed-order reductions, no floating-point atomics, so the
@@ -42,50 +44,25 @@ constexpr int PS_CT = PS_CW * 32;          // compute threads
 constexpr int PS_THREADS = PS_CT + 32;     // + one producer warp
 constexpr int PS_SL = PS_CW;               // K-slices of a GEMV stage, one per compute warp
 constexpr int PS_CBAR = 1;                 // named barrier of the compute warps
-#ifndef PS_SLOT_KB
-#define PS_SLOT_KB 64
-#endif
-constexpr int PS_SLOT = PS_SLOT_KB * 1024;  // bytes per ring slot
+constexpr int PS_SLOT = 64 * 1024;         // bytes per ring slot
 constexpr int PS_S = 196608 / PS_SLOT;      // ring slots (192 KB of shared memory)
 constexpr int PS_MAX_RPS = 32;
 constexpr int PS_MAX_RES = 64;
 constexpr int PS_RED_ROWS = 192;          // rows whose slice partials wait in shared memory
 constexpr int PS_AW = PS_CW;               // warps that compute attention
 constexpr int PS_MAX_NS = 64;              // attention splits per (row, kv head)
-constexpr uint32_t PS_SPIN = 1u << 22;     // polls of a grid-wide wait (each an L2 round trip)
+constexpr uint32_t PS_SPIN = 1u << 22;     // default polls of a grid-wide wait (each an L2 round trip)
 
 enum { PK_EMBED = 0, PK_QKV = 1, PK_ATTN = 2, PK_O = 3, PK_GU = 4, PK_DOWN = 5, PK_HEAD = 6 };
 // gate/up phase: a CTA owns gate rows [a, b) and up rows [a, b) and writes silu(gate) * up
 constexpr int EPI_SWIGLU_PAIR = 3;
 
-// Bounded wait on a ring barrier.  PS_WAIT_MODE 0: try_wait (may suspend for a
-// hardware-chosen time); 1: try_wait with a short suspend-time hint; 2: test_wait spin.
-#ifndef PS_WAIT_MODE
-#define PS_WAIT_MODE 0
-#endif
-__device__ __forceinline__ bool ps_wait(uint64_t* bar, uint32_t parity) {
-#if PS_WAIT_MODE == 0
-    return mbar_wait(bar, parity);
-#else
-    for (uint32_t i = 0; i < MBAR_POLLS * 4u; ++i) {
-        uint32_t ok;
-#if PS_WAIT_MODE == 1
-        asm volatile(
-            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
-            : "=r"(ok)
-            : "r"(smem_u32(bar)), "r"(parity), "r"(64u)
-            : "memory");
-#else
-        asm volatile(
-            "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-            : "=r"(ok)
-            : "r"(smem_u32(bar)), "r"(parity)
-            : "memory");
-#endif
-        if (ok) return true;
-    }
+// Bounded wait on a ring barrier: false after `polls` polls of try_wait (each
+// may suspend for a hardware-chosen time), never an endless spin.
+__device__ __forceinline__ bool ps_wait(uint64_t* bar, uint32_t parity, uint32_t polls) {
+    for (uint32_t i = 0; i < polls; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
     return false;
-#endif
 }
 
 __device__ __forceinline__ float4 ldcg4(const float* p) { return __ldcg(reinterpret_cast<const float4*>(p)); }
@@ -126,10 +103,11 @@ struct PsStage {
 
 // shared memory besides the ring; the GEMV and attention phases never overlap,
 // so their scratch shares one union
-// poll until *p >= target (acquire), giving up after PS_SPIN polls or when the
+// poll until *p >= target (acquire), giving up after `polls` polls or when the
 // grid-wide abort word is set; false if it gave up
-__device__ __forceinline__ bool ps_poll_ge(const unsigned* p, unsigned target, const volatile unsigned* abort_word) {
-    for (uint32_t i = 0; i < PS_SPIN; ++i) {
+__device__ __forceinline__ bool ps_poll_ge(const unsigned* p, unsigned target, const volatile unsigned* abort_word,
+                                           uint32_t polls) {
+    for (uint32_t i = 0; i < polls; ++i) {
         if (ld_acquire(p) >= target) return true;
         if ((i & 63u) == 63u && *abort_word) return false;
     }
@@ -141,6 +119,11 @@ struct PsShared {
     uint64_t full_bar[PS_S];   // a ring slot's copy landed (producer's expect_tx + the copy bytes)
     uint64_t empty_bar[PS_S];  // every compute warp is done with the slot
     int abort;
+    // wait bounds of this launch (the defaults unless a test shortened them) and
+    // the test hooks: a phase whose grid-wait target is one above the grid size,
+    // and a stage that CTA 0's producer never issues (-1: none)
+    uint32_t spin, ring_polls;
+    int hold_phase, drop_stage;
     float nrm[PS_CW];
     float wm[PS_AW][8], wl[PS_AW][8], wf[PS_AW][8];   // per (attention warp, head): max, sum, merge factor
     float hm[8], hl[8];                               // per head: the split's max and sum
@@ -371,7 +354,7 @@ struct PsState {
     __device__ const unsigned char* stage_wait() {
         const int slot = cons % PS_S;
         volatile int* ab = &sh.abort;
-        if (!*ab && !ps_wait(&sh.full_bar[slot], (cons / PS_S) & 1)) {
+        if (!*ab && !ps_wait(&sh.full_bar[slot], (cons / PS_S) & 1, sh.ring_polls)) {
             *ab = 1;
             atomicOr(P.err, FAULT_WAIT);
         }
@@ -385,39 +368,10 @@ struct PsState {
     }
     __device__ static void csync() { named_sync(PS_CBAR, PS_CT); }
 
-    // the bytes of stage s into L2 (a hint; no shared memory involved)
-    __device__ void prefetch(const PsStage& s) const {
-        if (s.kind != PK_ATTN) {
-            if (s.b0) prefetch_l2_bulk(s.s0, s.b0);
-            if (s.b1) prefetch_l2_bulk(s.s1, s.b1);
-            if (s.b2) prefetch_l2_bulk(s.s2, s.b2);
-            return;
-        }
-        const int l = s.layer, u = s.u;
-        const int sp = u % P.nsplit, g = (u / P.nsplit) % P.Hkv, r = u / (P.nsplit * P.Hkv);
-        const int j0 = sp * P.split_len;
-        const int j1 = min(j0 + P.split_len, P.cap);
-        const int p0 = j0 + s.uloc * PPS, p1 = min(p0 + PPS, j1);
-        const unsigned char* kb = static_cast<const unsigned char*>(P.kv[2 * l]);
-        const unsigned char* vb = static_cast<const unsigned char*>(P.kv[2 * l + 1]);
-        if (PAGED) {
-            for (int q = p0; q < p1; q += P.page) {
-                int pg = P.slot_map[(size_t)r * P.pages_per_row + q / P.page];
-                if (pg < 0 || pg >= P.num_pages) pg = 0;
-                const size_t off = (size_t)((pg * P.Hkv + g) * P.page) * HD * 2;
-                prefetch_l2_bulk(kb + off, (unsigned)(P.page * HD * 2));
-                prefetch_l2_bulk(vb + off, (unsigned)(P.page * HD * 2));
-            }
-        } else {
-            const size_t off = (size_t)((r * P.Hkv + g) * P.cap + p0) * HD * 2;
-            prefetch_l2_bulk(kb + off, (unsigned)((p1 - p0) * HD * 2));
-            prefetch_l2_bulk(vb + off, (unsigned)((p1 - p0) * HD * 2));
-        }
-    }
-
     // producer warp, lane 0: stream every stage of the CTA's step through the
     // ring; each stage is resolved while its slot is still in use, so a freed
-    // slot is refilled by the copy instructions alone
+    // slot is refilled by the copy instructions alone.  After an abort it issues
+    // nothing more and waits (bounded) for the copies it has in flight.
     __device__ void produce() {
         PsCursor c;
         c.p = 0;
@@ -425,45 +379,26 @@ struct PsState {
         c.nst = -1;
         PsStage s;
         volatile int* ab = &sh.abort;
+        const int dropped = cta == 0 ? sh.drop_stage : -1;   // test hook: a copy that never lands
         bool have = next(c, s);
-        // second cursor: while the producer waits for a slot (the compute warps
-        // are behind, e.g. at a phase dependency), it prefetches the stages after
-        // the pending one into L2, up to P.pf ahead, so HBM keeps streaming
-        PsCursor f = c;
-        PsStage sf;
-        int fi = 1;   // stage index next(f) yields
         int i = 0;
         for (; have && !*ab; ++i) {
             const int slot = i % PS_S;
             if (i >= PS_S) {
-                const uint32_t par = ((i / PS_S) - 1) & 1;
-                if (fi <= i) {   // f fell behind the ring: restart it after stage i
-                    f = c;
-                    fi = i + 1;
-                }
-                bool ok = false;
-                for (uint32_t it = 0; it < MBAR_POLLS; ++it) {
-                    if (mbar_try_wait(&sh.empty_bar[slot], par)) {
-                        ok = true;
-                        break;
-                    }
-                    if (P.pf > 0 && (it & 3u) == 3u && fi <= i + P.pf && next(f, sf)) {
-                        prefetch(sf);
-                        ++fi;
-                    }
-                }
-                if (!ok) {
+                if (!ps_wait(&sh.empty_bar[slot], ((i / PS_S) - 1) & 1, sh.ring_polls)) {
                     *ab = 1;
                     atomicOr(P.err, FAULT_WAIT);
                     break;
                 }
+                if (*ab) break;
             }
-            issue(s, slot);
+            if (i != dropped) issue(s, slot);
             have = next(c, s);
         }
         // no copy may still be landing when the CTA exits (after an abort some were never consumed)
         for (int j = max(0, i - PS_S); j < i; ++j)
-            if (!mbar_wait(&sh.full_bar[j % PS_S], (j / PS_S) & 1)) atomicOr(P.err, FAULT_WAIT);
+            if (j != dropped && !ps_wait(&sh.full_bar[j % PS_S], (j / PS_S) & 1, sh.ring_polls))
+                atomicOr(P.err, FAULT_WAIT);
     }
 
     __device__ void grid_arrive(int p) {
@@ -473,7 +408,8 @@ struct PsState {
     __device__ void grid_wait(int p) {
         if (tid == 0) {
             volatile unsigned* gab = P.bar + np + 1;
-            if (!ps_poll_ge(P.bar + p, (unsigned)nc, gab)) {
+            const unsigned target = (unsigned)nc + (p == sh.hold_phase ? 1u : 0u);
+            if (!ps_poll_ge(P.bar + p, target, gab, sh.spin)) {
                 sh.abort = 1;
                 atomicOr(P.err, FAULT_WAIT);
                 atomicExch(const_cast<unsigned*>(gab), 1u);
@@ -958,7 +894,7 @@ __device__ __forceinline__ void ps_attention(PsState<HD, G, PAGED>& st, int l) {
             red_release(cnt, 1u);
             const unsigned target = (unsigned)P.nsplit * (unsigned)(l + 1);
             volatile unsigned* gab = P.bar + st.np + 1;
-            if (!ps_poll_ge(cnt, target, gab)) {
+            if (!ps_poll_ge(cnt, target, gab, sh.spin)) {
                 sh.abort = 1;
                 atomicOr(P.err, FAULT_WAIT);
                 atomicExch(const_cast<unsigned*>(gab), 1u);
@@ -1021,6 +957,12 @@ __global__ void __launch_bounds__(PS_THREADS, 1) k_persist(const __grid_constant
             mbar_init(&sh.empty_bar[s], PS_CW);
         }
         sh.abort = 0;
+        // the wait bounds and test hooks of this launch (all zero: defaults, no hooks)
+        const uint4 dbg = __ldcg(reinterpret_cast<const uint4*>(P.dbg));
+        sh.spin = dbg.x ? dbg.x : PS_SPIN;
+        sh.ring_polls = dbg.y ? dbg.y : MBAR_POLLS;
+        sh.hold_phase = (int)dbg.z - 1;
+        sh.drop_stage = (int)dbg.w - 1;
         mbar_fence_init();
     }
     __syncthreads();
@@ -1179,7 +1121,6 @@ cudaError_t persist_plan(PersistPlan* plan, int num_sms) {
     if (bn == 0) return cudaErrorNotSupported;
     p.split_len = bl;
     p.nsplit = bn;
-    p.pf = 0;
     plan->grid = num_sms;
     plan->block = PS_THREADS;
     plan->smem = (size_t)PS_S * PS_SLOT + 1024;

@@ -66,6 +66,7 @@ typedef enum dec_status {
 #define DEC_FAULT_POS       0x2u  /* Pos[r] outside [0, cap) */
 #define DEC_FAULT_WRITE_MAP 0x4u  /* WriteMap[r] outside [0, num_pages * page_size) */
 #define DEC_FAULT_SLOT_MAP  0x8u  /* a SlotMap entry outside [0, num_pages) */
+#define DEC_FAULT_WAIT      0x10u /* an in-kernel wait on another CTA or on a copy gave up (bounded poll) */
 
 typedef enum dec_dtype { DEC_DTYPE_F32 = 0, DEC_DTYPE_BF16 = 1 } dec_dtype;
 
@@ -176,9 +177,13 @@ typedef struct dec_stats {
     int64_t kv_bytes;         /* device bytes of K and V over all layers */
 } dec_stats;
 
-/* Create a handle for `cfg` on cfg->device.  Validates the configuration
- * (DEC_E_INVALID / DEC_E_UNSUPPORTED naming the field) before touching the GPU.
- * *out receives the handle, or NULL on failure. */
+/* Create a handle for `cfg` on cfg->device ("Execution", executor contract:
+ * one engine per target, set up before any weight is bound; the handle plays
+ * the executor object and every later call goes through it).  Validates the
+ * configuration (DEC_E_INVALID / DEC_E_UNSUPPORTED naming the field, like the
+ * planner's refusals) before touching the GPU; DEC_E_CUDA if the device cannot
+ * be selected.  *out receives the handle, or NULL on failure; the caller owns
+ * it and releases it with dec_destroy. */
 int dec_init(const dec_config *cfg, dec_handle **out);
 
 /* Bind `n` weights by role ("Execution": load_weights(store, map)).  May be
@@ -189,7 +194,11 @@ int dec_init(const dec_config *cfg, dec_handle **out);
 int dec_load_weights(dec_handle *h, const dec_weight *w, size_t n);
 
 /* Device bytes that dec_capture needs for this shape (KV store, slots,
- * activations, attention partials, RoPE table). */
+ * activations, attention partials, RoPE table): the preallocated Storage::State
+ * buffers of capacity cap per layer plus the step's intermediates ("Execution",
+ * section "A constant-shape decode graph": K and V are preallocated to cap).
+ * Host-only (no device call).  *bytes (host) receives the size; DEC_E_INVALID
+ * for a configuration dec_init would refuse or a shape dec_capture would refuse. */
 int dec_workspace_size(const dec_config *cfg, int32_t cap, int32_t rows, int32_t kv_layout,
                        int32_t page_size, int32_t num_pages, size_t *bytes);
 
@@ -346,8 +355,13 @@ int dec_set_eager(dec_handle *h, int32_t eager);
 int dec_reset_state(dec_handle *h);
 
 /* Device address and byte size of one layer's K (which = 0) or V (which = 1)
- * store, in the layout of the capture's dec_kv_layout; for tests that pre-fill
- * or inspect the carried state. */
+ * store, in the layout of the capture's dec_kv_layout: the carried state that
+ * the pages' reference evaluation returns beside the primary output and that
+ * parity covers element by element ("Execution", section "Verification", tier
+ * 2: every output and carried state).  For tests that pre-fill or inspect it.
+ * *ptr (host) receives a device pointer owned by the handle (valid until
+ * dec_destroy); *bytes (host, optional) its size.  DEC_E_STATE before
+ * dec_capture, DEC_E_INVALID for a bad layer or which. */
 int dec_kv_ptr(dec_handle *h, int32_t layer, int32_t which, void **ptr, size_t *bytes);
 
 /* One layer's decode attention as a standalone operation, on the caller's
@@ -368,17 +382,23 @@ int dec_attention(dec_handle *h, int32_t layer, const float *qkv, const int32_t 
 /* dec_attention without any allocation.  Same operation, arguments and
  * results as dec_attention; the split scratch (partials and completion
  * counters) lives in a fixed device array inside the library instead of the
- * handle's workspace, so this call allocates nothing -- for callers that
- * cannot allocate where they run attention (inside a stream capture, from a
- * fixed device-memory budget, or where an allocation's implicit device
- * synchronisation is not acceptable).  The pages have no counterpart of this
- * entry point.
- * Limits: the array holds 2^19 fp32 partials and 1024 counters; a shape that
- * needs more returns DEC_E_UNSUPPORTED.  Every GPU that loads the library keeps
- * the array until the library is unloaded.  All calls on a device share the
- * array (it keeps the last call's contents; the counters are cleared on entry),
- * so calls that overlap on the GPU race.  The first call on a device looks up
- * the array's device address: make it before any stream capture. */
+ * handle's workspace, so this call allocates nothing.  It is for callers that
+ * cannot allocate device memory where they run attention: a serving process
+ * that reserved its whole device-memory budget up front (weights and KV cache
+ * sized to fill the GPU) and has nothing left to hand out per call, and code
+ * whose latency cannot absorb cudaMalloc / cudaFree, which may synchronise the
+ * whole device.  Like dec_attention it runs on the handle's stream and waits
+ * (bounded) for its result before returning.  The pages have no counterpart of
+ * this entry point.
+ * Limits: the array holds 2^19 fp32 partials and 1024 counters (about 2 MiB); a
+ * shape that needs more (rows * n_heads * splits * (head_dim + 4) floats)
+ * returns DEC_E_UNSUPPORTED and leaves the handle usable.  Every GPU that loads
+ * the library keeps the array until the process exits.  All calls on a device
+ * share the array (it keeps the last call's contents; the counters are cleared
+ * on entry), so calls that overlap on the GPU race: serialise them.  The first
+ * call on a device looks up the array's device address (once per device, kept
+ * for the life of the process; a cudaDeviceReset invalidates it together with
+ * every handle); make that first call before any stream capture. */
 int dec_attention_static(dec_handle *h, int32_t layer, const float *qkv, const int32_t *pos, float *out);
 
 /* Device address of the logits [rows, vocab] fp32 of the last step. */
@@ -387,7 +407,18 @@ int dec_logits_ptr(dec_handle *h, float **ptr);
 /* The CUDA stream the handle runs on (as a cudaStream_t). */
 int dec_stream(dec_handle *h, void **stream);
 
+/* Counters and state of the handle ("Execution", executor contract: stats).
+ * Copies a dec_stats snapshot into *out (host); touches no device and works on
+ * a poisoned handle.  DEC_E_INVALID for a NULL argument. */
 int dec_stats_get(const dec_handle *h, dec_stats *out);
+
+/* Device address of the paged read map [rows, cap / page_size] int32 (the
+ * Slot::SlotMap buffer that the recorded kernels read, "Execution", section
+ * "Slot buffers").  Introspection for tests: writing it directly bypasses
+ * dec_set_slot_map's host range check, so the kernels' own check
+ * (DEC_FAULT_SLOT_MAP) can be exercised.  Owned by the handle.  DEC_E_STATE
+ * for a contiguous capture or before dec_capture. */
+int dec_slot_map_ptr(dec_handle *h, int32_t **ptr);
 
 /* Profiling hook: launch kernel `index` of the recorded step sequence alone,
  * eagerly, on the handle's stream (no slot write, no wait).  Order: 0 embedding;
@@ -419,10 +450,38 @@ int dec_debug_busy(dec_handle *h, int64_t microseconds);
 /* Test hook: change the wait bound of an existing handle (ms, > 0). */
 int dec_set_timeout(dec_handle *h, int64_t wait_timeout_ms);
 
+/* Test hook for the in-kernel bounded waits of the persistent step ("Execution",
+ * section "Failure handling": every wait is bounded, and a wait that gives up
+ * is a typed error rather than a hang).  Takes effect from the next launch:
+ *   grid_polls  polls of a wait on other CTAs (phase counters, attention split
+ *               groups) before it gives up; 0: the default (2^22)
+ *   ring_polls  polls of a wait on a shared-memory ring stage (a copy landing,
+ *               a slot freed) before it gives up; 0: the default (2^22)
+ *   hold_phase  phase index whose grid-wide wait target is raised by one, so
+ *               that wait cannot complete and gives up after grid_polls
+ *               (phases: 0 embedding, 1 + 5l + {0 QKV, 1 attention, 2 O-proj,
+ *               3 gate/up, 4 down} of layer l, 5L + 1 head); -1: none
+ *   drop_stage  ring stage index (counted over the whole step) that CTA 0's
+ *               producer never issues, so its consumers give up after
+ *               ring_polls; -1: none
+ * A wait that gives up sets DEC_FAULT_WAIT in the error word; the kernel then
+ * skips the remaining work, waits (bounded) for its own copies in flight and
+ * exits; the step returns DEC_E_DEVICE_FAULT and the handle needs
+ * dec_reset_state.  (0, 0, -1, -1) restores the defaults.  DEC_E_STATE unless
+ * the capture uses DEC_STRATEGY_PERSISTENT; DEC_E_INVALID for hold_phase or
+ * drop_stage below -1. */
+int dec_debug_wait(dec_handle *h, uint32_t grid_polls, uint32_t ring_polls, int32_t hold_phase, int32_t drop_stage);
+
 const char *dec_last_error(const dec_handle *h);
 const char *dec_status_str(int status);
 
-/* Free everything the library allocated (after a bounded wait for the stream). */
+/* Release the handle ("Execution", executor contract: unload): after a
+ * bounded wait for its stream, free everything the library allocated (graph,
+ * library-owned workspace, pinned staging, stream and event).  Borrowed
+ * weights and a caller workspace are not touched.  A poisoned handle frees
+ * only host state and leaks the device memory that pending work could
+ * reference ("Execution", section "Failure handling").  DEC_E_INVALID for
+ * NULL; the handle is invalid afterwards whatever the status. */
 int dec_destroy(dec_handle *h);
 
 #ifdef __cplusplus

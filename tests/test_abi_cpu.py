@@ -110,7 +110,7 @@ def test_every_handle_call_refuses_a_null_handle(lib):
             continue
         args = []
         for t in argtypes:
-            if t in (C.c_int32, C.c_int64, C.c_size_t, C.c_int):
+            if t in (C.c_int32, C.c_int64, C.c_size_t, C.c_int, C.c_uint32):
                 args.append(1)
             else:
                 args.append(None)

@@ -1,12 +1,16 @@
 """The allocation-free attention entry point (dec_attention_static).
 
-Callers that cannot allocate device memory where they run attention (inside a
-stream capture, on a fixed memory budget, or where cudaMalloc's implicit device
-synchronisation is not acceptable) use dec_attention_static, which keeps its
-split scratch in a fixed array inside the library.  It must give the same
-results as dec_attention, which uses the handle's workspace, call after call:
-the array keeps the previous call's contents, so a second call in a row checks
-that nothing stale leaks into the result.  This file is collected last.
+Some callers cannot allocate device memory where they run attention: a serving
+process that reserved its whole device-memory budget up front, or a loop whose
+latency cannot absorb cudaMalloc / cudaFree (which may synchronise the whole
+device).  dec_attention_static keeps its split scratch in a fixed array inside
+the library instead.  It must give the same results as dec_attention, which
+uses the handle's workspace, call after call: the array keeps the previous
+call's contents, so a second call in a row checks that nothing stale leaks into
+the result.  After its first call on a device (which resolves the array's
+address and may load the library's module), it must not change the device's
+free memory.  A shape whose scratch exceeds the array is refused and leaves the
+handle usable.  This file is collected last.
 """
 import numpy as np
 import pytest
@@ -35,12 +39,45 @@ def test_static_scratch_attention_matches_workspace_attention(name, rows):
     ref = torch.empty(rows, wl.q_dim, dtype=torch.float32, device="cuda:0")
     dec.attention(1, qkv, pos, ref)   # existing entry point: scratch in the workspace
     ref_h = ref.cpu().numpy()
-    for call in range(2):
-        out = torch.full((rows, wl.q_dim), float("nan"), dtype=torch.float32, device="cuda:0")
+    outs = [torch.full((rows, wl.q_dim), float("nan"), dtype=torch.float32, device="cuda:0") for _ in range(3)]
+    torch.cuda.synchronize()
+    free_after_first = None
+    for call in range(3):
         dec._after_torch()
-        rc = B.dec_attention_static(dec.h, 1, qkv.data_ptr(), pos.data_ptr(), out.data_ptr())
+        rc = B.dec_attention_static(dec.h, 1, qkv.data_ptr(), pos.data_ptr(), outs[call].data_ptr())
         assert rc == B.DEC_OK, B.last_error(dec.h)
-        got = out.cpu().numpy()
+        torch.cuda.synchronize()
+        free_now = torch.cuda.mem_get_info()[0]
+        if call == 0:
+            free_after_first = free_now
+        else:
+            assert free_now == free_after_first, "dec_attention_static changed the device's free memory"
+        got = outs[call].cpu().numpy()
         for r in range(rows):
             assert_close(got[r], ref_h[r], wl, f"static-scratch attention, call {call}, row {r}")
+    dec.close()
+
+
+def test_static_scratch_refuses_a_shape_beyond_the_array():
+    """8 rows x 192 kv heads need 1536 split-completion counters, more than the
+    array's 1024: refused with DEC_E_UNSUPPORTED before any device work; the
+    handle then runs dec_attention as before."""
+    import torch
+    from graph_replay_gb300 import _binding as B
+
+    wl = gen.WORKLOADS["1b"].replace(name="noalloc_wide", n_layers=1, d_model=1024, n_heads=192, n_kv_heads=192,
+                                     head_dim=64, ffn_hidden=1024, vocab=256, cap=64, rows=8)
+    dec, _ = make_decoder(wl)
+    qkv = torch.from_numpy(gen.normal(wl.seed, 92, (wl.rows, wl.q_dim + 2 * wl.kv_dim), sigma=1.0,
+                                      dtype="f32")).cuda()
+    pos = torch.arange(wl.rows, dtype=torch.int32, device="cuda:0")
+    out = torch.zeros(wl.rows, wl.q_dim, dtype=torch.float32, device="cuda:0")
+    dec._after_torch()
+    rc = B.dec_attention_static(dec.h, 0, qkv.data_ptr(), pos.data_ptr(), out.data_ptr())
+    assert rc == B.DEC_E_UNSUPPORTED
+    assert "fixed" in B.last_error(dec.h)
+    assert dec.stats()["state"] == 0
+    assert torch.count_nonzero(out).item() == 0        # nothing was written
+    dec.attention(0, qkv, pos, out)                    # the handle still works
+    assert torch.isfinite(out).all().item()
     dec.close()
