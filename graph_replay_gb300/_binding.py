@@ -80,6 +80,7 @@ _SIG = [
     ("dec_wait", ctypes.c_int, [_P, _P, _P, _P]),
     ("dec_chain", ctypes.c_int, [_P, _I32, _P, _P, _P, _P]),
     ("dec_prefill", ctypes.c_int, [_P, _P, _P, _I32, _I32, _P, _P]),
+    ("dec_prefill_block", ctypes.c_int, [_P, _I32, _P, _P, _I32, _I32, _P, _P]),
     ("dec_set_sampler", ctypes.c_int, [_P, _P]),
     ("dec_logprobs", ctypes.c_int, [_P, _I32, _P, _P]),
     ("dec_set_strategy", ctypes.c_int, [_P, _I32]),
@@ -224,6 +225,10 @@ def dec_logprobs(h, n: int, ids_ptr, vals_ptr) -> int:
 
 def dec_prefill(h, pages_ptr, tokens_ptr, n: int, pos0: int, logits_ptr, id_ptr) -> int:
     return lib().dec_prefill(h, pages_ptr, tokens_ptr, n, pos0, logits_ptr, id_ptr)
+
+
+def dec_prefill_block(h, row: int, pages_ptr, tokens_ptr, n: int, pos0: int, logits_ptr, id_ptr) -> int:
+    return lib().dec_prefill_block(h, row, pages_ptr, tokens_ptr, n, pos0, logits_ptr, id_ptr)
 
 
 def dec_set_strategy(h, strategy: int) -> None:

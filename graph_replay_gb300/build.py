@@ -13,7 +13,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libgraphdec.so")
-SOURCES = ["engine.cu", "gemv.cu", "gemv_bf16.cu", "gemv_f32.cu", "gemv_tc.cu", "gemv_tma.cu", "attn.cu", "attn_mma.cu", "misc.cu", "sample.cu", "noalloc.cu", "persist.cu"]
+SOURCES = ["engine.cu", "gemv.cu", "gemv_bf16.cu", "gemv_f32.cu", "gemv_tc.cu", "gemv_tma.cu", "attn.cu", "attn_mma.cu", "misc.cu", "sample.cu", "noalloc.cu", "persist.cu", "prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -168,6 +168,8 @@ struct dec_handle {
     std::vector<AttnPlan> attn;   // 1 per layer
     int kernels = 0;
 
+    PrefillState* pf = nullptr;    // block prefill buffers (created by the first dec_prefill_block)
+
     cudaGraph_t graph = nullptr;
     cudaGraphExec_t exec = nullptr;
     size_t nodes = 0;
@@ -1007,6 +1009,73 @@ int dec_prefill(dec_handle* h, const int32_t* pages, const int32_t* tokens, int3
     return DEC_OK;
 }
 
+int dec_prefill_block(dec_handle* h, int32_t row, const int32_t* pages, const int32_t* tokens, int32_t n, int32_t pos0,
+                      float* logits_out, int32_t* id_out) {
+    int rc = gate(h, true);
+    if (rc) return rc;
+    if (h->state == ST_NEEDS_RESET) return fail(h, DEC_E_NEEDS_RESET, "an earlier step failed; call dec_reset_state");
+    const dec_config& c = h->cfg;
+    if (c.weight_dtype != DEC_DTYPE_BF16 || c.kv_dtype != DEC_DTYPE_BF16)
+        return fail(h, DEC_E_UNSUPPORTED, "the block prefill needs bf16 weights and K/V");
+    PrefillArgs a{};
+    a.L = c.n_layers; a.d = c.d_model; a.Hq = c.n_heads; a.Hkv = c.n_kv_heads; a.hd = c.head_dim;
+    a.F = c.ffn_hidden; a.cap = h->cap; a.eps = (float)c.rms_eps;
+    a.embed = h->embed;
+    a.lw = reinterpret_cast<const void* const*>(h->lw.data());
+    a.K = h->K.data();
+    a.V = h->V.data();
+    a.paged = h->layout == DEC_KV_PAGED;
+    a.page = h->page;
+    a.ppr = h->ppr;
+    a.rope = h->d_rope;
+    a.err = &h->d_status->err;
+    if (!prefill_supported(a))
+        return fail(h, DEC_E_UNSUPPORTED, "no block prefill for this shape (head_dim 64 or 128, n_heads / n_kv_heads "
+                    "2 or 4, d_model, n_heads * head_dim and ffn_hidden multiples of 64)");
+    if (!tokens || (a.paged && !pages)) return fail(h, DEC_E_INVALID, "tokens (and for paged K/V the pages) are required");
+    if (!a.paged && (row < 0 || row >= h->rows)) return fail(h, DEC_E_RANGE, "row %d outside [0, %d)", row, h->rows);
+    if (n < 1 || pos0 < 0 || (int64_t)pos0 + n > h->cap)
+        return fail(h, DEC_E_RANGE, "positions [%d, %d) outside [0, %d)", pos0, pos0 + n, h->cap);
+    for (int i = 0; i < n; ++i)
+        if (tokens[i] < 0 || tokens[i] >= c.vocab)
+            return fail(h, DEC_E_RANGE, "tokens[%d] = %d outside [0, %d)", i, tokens[i], c.vocab);
+    if (a.paged)
+        for (int i = 0; i < h->ppr; ++i)
+            if (pages[i] < 0 || pages[i] >= h->npages)
+                return fail(h, DEC_E_RANGE, "pages[%d] = %d outside [0, %d)", i, pages[i], h->npages);
+    if ((rc = bounded_wait(h)) != DEC_OK) return rc;   // no step in flight
+    cudaError_t e;
+    if (!h->pf) {
+        e = prefill_create(a, h->num_sms, &h->pf);
+        if (e == cudaErrorMemoryAllocation) return fail(h, DEC_E_OOM, "block prefill buffers: device allocation failed");
+        if (e != cudaSuccess) return cuda_fail(h, e, "block prefill setup");
+    }
+    // the last token's hidden state goes through the step's own head as row 0
+    if ((e = cudaMemsetAsync(h->d_status, 0, sizeof(StatusBlock), h->stream)) != cudaSuccess)
+        return cuda_fail(h, e, "status clear");
+    if ((e = prefill_run(h->pf, tokens, n, pos0, row, pages, h->d_x, h->stream)) != cudaSuccess)
+        return cuda_fail(h, e, "block prefill");
+    if ((e = gemv_launch(h->gemv.back(), h->stream, false)) != cudaSuccess) return cuda_fail(h, e, "prefill head");
+    if ((e = cudaMemcpyAsync(h->h_status, h->d_status, sizeof(StatusBlock), cudaMemcpyDeviceToHost, h->stream)) !=
+        cudaSuccess)
+        return cuda_fail(h, e, "status readback");
+    if (logits_out && (e = cudaMemcpyAsync(h->h_logits, h->d_logits, sizeof(float) * c.vocab, cudaMemcpyDeviceToHost,
+                                           h->stream)) != cudaSuccess)
+        return cuda_fail(h, e, "logits readback");
+    if ((rc = bounded_wait(h)) != DEC_OK) return rc;
+    if (h->h_status->err) {
+        h->last_fault = h->h_status->err;
+        h->state = ST_NEEDS_RESET;
+        return fail(h, DEC_E_DEVICE_FAULT, "device check failed in the prefill (error word 0x%x)", h->h_status->err);
+    }
+    if (logits_out) memcpy(logits_out, h->h_logits, sizeof(float) * c.vocab);
+    if (id_out) {
+        const unsigned long long k = h->h_status->amax[0];
+        *id_out = k ? (int32_t)(0xFFFFFFFFu - (uint32_t)(k & 0xFFFFFFFFull)) : -1;
+    }
+    return DEC_OK;
+}
+
 int dec_set_sampler(dec_handle* h, const dec_sampler* sp) {
     int rc = gate(h, false);
     if (rc) return rc;
@@ -1358,6 +1427,7 @@ int dec_destroy(dec_handle* h) {
         if (h->own_stream && h->stream) cudaStreamDestroy(h->stream);
     }
     // a poisoned handle leaks what the pending work could reference
+    if (device_idle) prefill_free(h->pf);
     for (auto& a : h->attn) attn_mma_release(a);
     delete h;
     return DEC_OK;

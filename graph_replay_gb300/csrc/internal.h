@@ -244,6 +244,31 @@ size_t persist_tmap_bytes(int n_layers);
 cudaError_t persist_tmaps(const PersistParams& p, void* const* kv, void* host_out);
 cudaError_t persist_launch(const PersistPlan& plan, cudaStream_t s);
 
+// ---------------- multi-token prefill of one sequence (prefill.cu) ----------------
+struct PrefillArgs {
+    int L, d, Hq, Hkv, hd, F, cap;
+    float eps;
+    const void* embed;          // [V, d] bf16
+    const void* const* lw;      // host array [L * 9] of device pointers: attn_norm, q, k, v, o, ffn_norm, gate, up, down
+    void* const* K;             // host array [L] of device pointers: K store of each layer
+    void* const* V;             // host array [L]: V store
+    bool paged;
+    int page, ppr;              // paged: tokens per page, pages per sequence
+    const float2* rope;         // device [cap, hd / 2]
+    unsigned* err;              // device error word
+};
+struct PrefillState;
+// whether this shape has a block prefill (bf16 weights and K/V are the caller's check)
+bool prefill_supported(const PrefillArgs& a);
+// device buffers and tensor maps of the block prefill (cudaMalloc; freed by prefill_free)
+cudaError_t prefill_create(const PrefillArgs& a, int num_sms, PrefillState** out);
+void prefill_free(PrefillState* s);
+// n tokens (host) at positions pos0 .. pos0 + n - 1 of sequence `row` (contiguous
+// K/V) or of the sequence on `pages` (host, paged K/V): every layer's K/V of those
+// positions written; the last token's hidden state (fp32 [d]) to x_last (device)
+cudaError_t prefill_run(PrefillState* s, const int* tokens, int n, int pos0, int row, const int* pages, float* x_last,
+                        cudaStream_t st);
+
 }  // namespace gd
 
 struct dec_handle;

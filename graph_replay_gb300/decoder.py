@@ -154,6 +154,19 @@ class Decoder:
         B.check(self.h, B.dec_prefill(self.h, _ptr(pg), _ptr(tk), int(tk.size), int(pos0), _ptr(logits), _ptr(idv)))
         return logits, int(idv[0])
 
+    def prefill_block(self, tokens, pos0: int = 0, row: int = 0, pages=None):
+        """Block prefill of one sequence (tensor-core projections, causal attention
+        over the block): row's contiguous K/V, or the sequence on `pages` (paged).
+        Returns (logits [vocab] after the last token, greedy id)."""
+        tk = np.ascontiguousarray(tokens, dtype=np.int32).reshape(-1)
+        pg = None if pages is None else np.ascontiguousarray(pages, dtype=np.int32).reshape(-1)
+        logits = np.empty(self.vocab, dtype=np.float32)
+        idv = np.zeros(1, dtype=np.int32)
+        self._after_torch()
+        B.check(self.h, B.dec_prefill_block(self.h, int(row), _ptr(pg), _ptr(tk), int(tk.size), int(pos0),
+                                            _ptr(logits), _ptr(idv)))
+        return logits, int(idv[0])
+
     def set_sampler(self, **params) -> None:
         """New sampler parameters for the coming steps (the decoder must have been
         built with a sampler); see make_sampler for the fields."""

@@ -296,6 +296,37 @@ int dec_chain(dec_handle *h, int32_t n_steps, const int32_t *tokens, const int32
 int dec_prefill(dec_handle *h, const int32_t *pages, const int32_t *tokens, int32_t n, int32_t pos0,
                 float *logits_out, int32_t *id_out);
 
+/* Multi-token prefill of ONE sequence as a block step ("Models, Registry and
+ * the Driver", section "The Model": a step shape is rows x new tokens;
+ * positions are absolute, so a prefill is a step continuing from a position).
+ * The n tokens at positions pos0 .. pos0 + n - 1 run in blocks of 128 tokens:
+ * per layer the projections are dense contractions on the tensor cores
+ * (tcgen05.mma, bf16 weights, activations as bf16 hi + lo parts, fp32
+ * accumulation), attention is causal over every position up to each token
+ * (online softmax, fp32), and every layer's K/V of the n positions is written
+ * into the sequence's store (rounded to bf16).  The last token's hidden state
+ * then goes through the captured step's final RMSNorm, LM head and argmax.
+ *   row         contiguous K/V: the capture row whose store holds the
+ *               sequence (0 .. rows-1); ignored for paged K/V
+ *   pages       paged K/V: host [cap / page_size] page ids of the sequence, each
+ *               in [0, num_pages); NULL for contiguous K/V
+ *   tokens      host [n], each in [0, vocab)
+ *   pos0        first position; pos0 + n <= cap (DEC_E_RANGE otherwise)
+ *   logits_out  host [vocab] fp32 logits after the last token, or NULL
+ *   id_out      host, the greedy id after the last token, or NULL
+ * Positions before pos0 must already hold the sequence's K/V (from steps or an
+ * earlier prefill).  Any capture with bf16 weights and K/V whose shape has
+ * head_dim 64 or 128, n_heads / n_kv_heads of 2 or 4, and d_model, n_heads *
+ * head_dim and ffn_hidden multiples of 64 (DEC_E_UNSUPPORTED otherwise).  The
+ * first call allocates the block's device buffers (cudaMalloc, kept until
+ * dec_destroy); the call is synchronous (bounded wait) and must not be
+ * captured.  Results agree with stepping the tokens one at a time within the
+ * parity tolerances, not bit for bit (other arithmetic, other summation
+ * order).  The captured step's slot buffers are untouched; its logits buffer
+ * holds this call's logits afterwards. */
+int dec_prefill_block(dec_handle *h, int32_t row, const int32_t *pages, const int32_t *tokens, int32_t n,
+                      int32_t pos0, float *logits_out, int32_t *id_out);
+
 /* Sampling suffix beyond greedy ("Models, Registry and the Driver", section
  * "The Driver": Head::Sample -- greedy or temperature / top-k / top-p /
  * min-p, optional top-n logprobs).  For each row of a step:
