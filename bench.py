@@ -371,12 +371,59 @@ def run_ours(args, rank, world, local_rank):
                 print(f"  {k:5s} x{v['phases']:<3d} {v['us_mean']:8.2f} us  {v['gbs']:7.1f} GB/s  "
                       f"end spread {v['end_spread_us']:6.2f} us  wait latency {v['wait_latency_us']:5.2f} us",
                       file=sys.stderr)
+    if world == 1 and args.prefill_tokens > 0 and wl.wdtype == "bf16":
+        out["prefill"] = prefill_leg(dec, wl, args.prefill_tokens)
     dec.close()
     if persistent and world == 1 and not args.no_graph_leg:
         out["graph_strategy"] = graph_strategy_leg(args, wl, cfg, w, slot_map, dev_slots, hbm_peak)
     if mw is not None and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(wl, mw, plist, toks, seconds=args.cpu_seconds)
     return out
+
+
+def prefill_leg(dec, wl, n_tokens, reps=3) -> dict:
+    """Block prefill of one sequence (dec_prefill_block) on the same decoder,
+    after the decode measurements: n_tokens prompt tokens at positions 0..n-1 of
+    row 0 (or the first pages), timed with CUDA events on the handle's stream
+    around the call (which waits for its own work).  Tensor-core work: every
+    128-token block multiplies each weight once by 256 bf16 activation rows
+    (the tokens' hi and lo parts), so the executed MMA work is twice the useful
+    2 x tokens x projection-parameters."""
+    import torch
+    import gen
+    n = min(int(n_tokens), wl.cap)
+    toks = gen.ints(wl.seed, 0x77, 0, wl.vocab, n).astype(np.int32)
+    pages = None
+    if wl.layout == "paged":
+        pages = np.arange(wl.cap // wl.page_size, dtype=np.int32)
+    dec.prefill_block(toks, 0, pages=pages)   # first call: buffers, tensor maps
+    stream = dec.stream()
+    times = []
+    for _ in range(reps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        dec.prefill_block(toks, 0, pages=pages)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    ms = float(np.median(times))
+    qd, kvd = wl.n_heads * wl.head_dim, wl.n_kv_heads * wl.head_dim
+    proj_params = wl.n_layers * ((qd + 2 * kvd) * wl.d_model + wl.d_model * qd + 3 * wl.ffn_hidden * wl.d_model)
+    blocks = (n + 127) // 128
+    useful = 2.0 * n * proj_params
+    executed = 2.0 * 256 * blocks * proj_params
+    try:
+        peak = float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["bf16_tflops"])
+    except Exception:
+        peak = 1900.0
+    return {"tokens": n, "ms": round(ms, 3), "tokens_per_s": round(n / (ms * 1e-3), 1),
+            "useful_tflops": round(useful / (ms * 1e-3) / 1e12, 2),
+            "mma_tflops": round(executed / (ms * 1e-3) / 1e12, 2),
+            "mma_frac_of_bf16_peak": round(executed / (ms * 1e-3) / 1e12 / peak, 4), "bf16_peak_tflops": peak,
+            "note": "whole dec_prefill_block call (projections, attention, norms, K/V writes, head); "
+                    "attention runs on the tensor cores too (mma.sync, bf16 hi/lo queries), "
+                    "its work not counted in the TFLOP/s figures"}
 
 
 def graph_strategy_leg(args, wl, cfg, w, slot_map, dev_slots, hbm_peak) -> dict:
@@ -480,6 +527,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefill-tokens", type=int, default=1024,
+                    help="tokens of the block-prefill leg timed after the decode line (0: skip)")
     ap.add_argument("--no-graph-leg", action="store_true",
                     help="skip timing the multi-kernel graph strategy beside the persistent line")
     ap.add_argument("--strategy", default="persistent", choices=["graph", "persistent"],

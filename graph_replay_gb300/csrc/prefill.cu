@@ -28,10 +28,7 @@ namespace gd {
 
 namespace {
 
-constexpr int PF_NT = 256;         // threads of the per-token kernels
-constexpr int PF_QB = 8;           // query tokens per attention CTA
-constexpr int PF_KT = 16;          // keys per attention tile
-constexpr int PF_AT = 256;         // attention threads: 32 query rows x 8
+constexpr int PF_NT = 1024;        // threads of the per-token kernels
 
 // hi / lo bf16 rows of one activation value (row t of the block and row PF_T + t)
 __device__ __forceinline__ void put_hilo(__nv_bfloat16* hb, int K, int t, int k, float v) {
@@ -70,6 +67,7 @@ __global__ void k_pf_resid_norm(float* x, const float* part, int splits, int d, 
     for (int i = threadIdx.x; i < d; i += blockDim.x) {
         float v = xr[i];
         if (part && t < nt) {
+#pragma unroll 4
             for (int s = 0; s < splits; ++s) v += part[((size_t)s * PF_T + t) * d + i];
             xr[i] = v;
         }
@@ -106,6 +104,7 @@ __global__ void k_pf_qkv(const float* part, int splits, int Hq, int nt, int pos0
     const float2* rt = rope + (size_t)pos * h2;
     auto val = [&](int n) {
         float v = 0.f;
+#pragma unroll 4
         for (int s = 0; s < splits; ++s) v += part[((size_t)s * PF_T + t) * N + n];
         return v;
     };
@@ -131,91 +130,153 @@ __global__ void k_pf_qkv(const float* part, int splits, int Hq, int nt, int pos0
     }
 }
 
-// Causal attention of PF_QB query tokens x the G query heads of kv head g over
-// positions [0, pos(token)], flash-style: key tiles of PF_KT, online softmax
-// per query row, fp32.  Query row r = token * G + head (32 rows at G = 4, 16 at
-// G = 2); 256 / rows threads per row.  The output goes to hb as the O
-// projection's hi/lo activation rows.
+// Causal attention on the tensor cores (mma.sync m16n8k16, bf16 in, fp32
+// accumulate), flash-style.  A CTA takes 64 query rows -- PF_QR / G tokens x
+// the G query heads of kv head g, row r = token * G + head -- and sweeps the
+// keys [0, last position of its tokens] in tiles of PF_KT2 keys.  Warp w owns
+// query rows 8w..8w+7: the MMA's 16 A rows hold their bf16 parts (rows 0-7) and
+// remainders (rows 8-15), so q keeps about 16 significant bits; S = Q K^T comes
+// out as hi + lo row pairs, and P (online softmax, fp32) goes back into the
+// next MMA's A fragments the same way, straight from the registers.  K and V
+// tiles are staged in shared memory (rows padded by 16 bytes: conflict-free
+// ldmatrix); V is read transposed.  The output goes to hb as the O projection's
+// hi/lo activation rows.
+constexpr int PF_QR = 64;          // query rows per CTA
+constexpr int PF_KT2 = 64;         // keys per tile
 template <int HD, int G>
-__global__ void __launch_bounds__(PF_AT) k_pf_attn(const float* q, int Hq, int nt, int pos0, float scale, PfKv kv,
-                                                   __nv_bfloat16* hb) {
-    constexpr int NR = PF_QB * G;           // query rows
-    constexpr int TPR = PF_AT / NR;         // threads per row
-    constexpr int KPT = PF_KT / TPR;        // keys per thread
-    constexpr int DPT = HD / TPR;           // output dims per thread
-    static_assert(NR * TPR == PF_AT && KPT * TPR == PF_KT && DPT * TPR == HD, "attention thread layout");
-    __shared__ float qs[NR][HD];
-    __shared__ float ks[PF_KT][HD + 1];
-    __shared__ float vs[PF_KT][HD];
-    __shared__ float ps[NR][PF_KT];
-    const int g = blockIdx.y, t0 = blockIdx.x * PF_QB, tid = threadIdx.x;
-    const int r = tid / TPR, sub = tid % TPR;
-    const int tq = t0 + r / G, hq = g * G + r % G;
-    const bool row_live = tq < nt;
-    const int qpos = pos0 + tq;
+__global__ void __launch_bounds__(256) k_pf_attn_mma(const float* q, int Hq, int nt, int pos0, float scale, PfKv kv,
+                                                     __nv_bfloat16* hb) {
+    constexpr int KS = HD / 16;            // k-steps of S = Q K^T
+    constexpr int DT = HD / 8;             // n-tiles of O
+    constexpr int NT = PF_KT2 / 8;         // n-tiles of S
+    constexpr int RS = HD + 8;             // shared row stride (bf16)
+    constexpr int TPC = PF_QR / G;         // tokens per CTA
+    __shared__ __align__(16) __nv_bfloat16 ks[PF_KT2 * RS];
+    __shared__ __align__(16) __nv_bfloat16 vs[PF_KT2 * RS];
+    const int g = blockIdx.y, t0 = blockIdx.x * TPC, tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tq = lane & 3;
     const int qd = Hq * HD;
-    for (int i = tid; i < NR * HD; i += PF_AT) {
-        const int rr = i / HD, e = i % HD, tt = t0 + rr / G, hh = g * G + rr % G;
-        qs[rr][e] = tt < nt ? q[(size_t)tt * qd + hh * HD + e] * scale : 0.f;
-    }
-    float o[DPT];
+    // this lane's query row (warp row gq) and its position
+    const int r = warp * 8 + gq, tok = t0 + r / G, head = g * G + r % G;
+    const bool live = tok < nt;
+    const int qpos = pos0 + tok;
+    // Q fragments: rows 0-7 bf16(q * scale), rows 8-15 the remainders
+    uint32_t qa[KS][4];
+    {
+        const float* qr = q + (size_t)tok * qd + head * HD;
 #pragma unroll
-    for (int e = 0; e < DPT; ++e) o[e] = 0.f;
+        for (int k = 0; k < KS; ++k) {
+            float v[4];
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) v[2 * h + e] = live ? qr[16 * k + 8 * h + 2 * tq + e] * scale : 0.f;
+            const float h0 = bf16_round_f(v[0]), h1 = bf16_round_f(v[1]), h2 = bf16_round_f(v[2]), h3 = bf16_round_f(v[3]);
+            qa[k][0] = pack_bf16x2(h0, h1);
+            qa[k][1] = pack_bf16x2(v[0] - h0, v[1] - h1);
+            qa[k][2] = pack_bf16x2(h2, h3);
+            qa[k][3] = pack_bf16x2(v[2] - h2, v[3] - h3);
+        }
+    }
+    float o[DT][4];
+#pragma unroll
+    for (int n = 0; n < DT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
     float m_run = -INFINITY, l_run = 0.f;
-    const int last = pos0 + min(t0 + PF_QB, nt) - 1;   // the last key any row of the CTA sees
-    for (int j0 = 0; j0 <= last; j0 += PF_KT) {
+    const int last = pos0 + min(t0 + TPC, nt) - 1;               // the last key any row of the CTA sees
+    const int wlast = pos0 + min(t0 + (warp * 8 + 7) / G + 1, nt) - 1;   // ... any row of this warp
+    for (int j0 = 0; j0 <= last; j0 += PF_KT2) {
         __syncthreads();
-        for (int i = tid; i < PF_KT * HD; i += PF_AT) {
-            const int kk = i / HD, e = i % HD, j = j0 + kk;
-            float kv_k = 0.f, kv_v = 0.f;
+        for (int i = tid; i < PF_KT2 * (HD / 8); i += 256) {     // 16-byte vectors of K and V
+            const int kk = i / (HD / 8), c = i % (HD / 8), j = j0 + kk;
+            uint4 kv4 = make_uint4(0u, 0u, 0u, 0u), vv4 = make_uint4(0u, 0u, 0u, 0u);
             if (j <= last) {
-                const size_t off = kv_off(kv, g, j);
-                kv_k = __bfloat162float(kv.K[off + e]);
-                kv_v = __bfloat162float(kv.V[off + e]);
+                const size_t off = kv_off(kv, g, j) + (size_t)c * 8;
+                kv4 = *reinterpret_cast<const uint4*>(kv.K + off);
+                vv4 = *reinterpret_cast<const uint4*>(kv.V + off);
             }
-            ks[kk][e] = kv_k;
-            vs[kk][e] = kv_v;
+            *reinterpret_cast<uint4*>(ks + kk * RS + c * 8) = kv4;
+            *reinterpret_cast<uint4*>(vs + kk * RS + c * 8) = vv4;
         }
         __syncthreads();
-        // scores of this thread's keys (sub, sub + TPR, ...)
-        float sc[KPT];
+        if (j0 > wlast) continue;   // every row of this warp is past these keys (masked)
+        // S = Q K^T: 16 rows x PF_KT2 keys
+        float sacc[NT][4];
+#pragma unroll
+        for (int n = 0; n < NT; ++n) sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.f;
+        const int mi = lane >> 3, rr = lane & 7;
+#pragma unroll
+        for (int k = 0; k < KS; ++k)
+#pragma unroll
+            for (int n2 = 0; n2 < NT / 2; ++n2) {   // two n-tiles (16 keys) per ldmatrix
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(smem_u32(ks + (16 * n2 + rr + ((mi >> 1) << 3)) * RS + 16 * k + ((mi & 1) << 3)), b0, b1, b2, b3);
+                mma_bf16(sacc[2 * n2], qa[k], b0, b1);
+                mma_bf16(sacc[2 * n2 + 1], qa[k], b2, b3);
+            }
+        // scores of row gq (hi + lo rows), keys 8n + 2tq + e; online softmax over the tile
+        float sc[NT][2];
         float mx = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < KPT; ++c) {
-            const int kk = sub + c * TPR, j = j0 + kk;
-            float s = 0.f;
-#pragma unroll 8
-            for (int e = 0; e < HD; ++e) s = fmaf(qs[r][e], ks[kk][e], s);
-            sc[c] = (row_live && j <= qpos) ? s : -INFINITY;
-            mx = fmaxf(mx, sc[c]);
-        }
+        for (int n = 0; n < NT; ++n)
 #pragma unroll
-        for (int w = 1; w < TPR; w <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, w));
+            for (int e = 0; e < 2; ++e) {
+                const int j = j0 + 8 * n + 2 * tq + e;
+                const float v = sacc[n][e] + sacc[n][2 + e];
+                sc[n][e] = (live && j <= qpos) ? v : -INFINITY;
+                mx = fmaxf(mx, sc[n][e]);
+            }
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
         const float mn = fmaxf(m_run, mx);
         const float alpha = m_run == -INFINITY ? 0.f : expf(m_run - mn);
-        float psum = 0.f;
+        float ps = 0.f;
+        // P as A fragments: per 16 keys (n-tiles 2kk, 2kk+1), rows 0-7 bf16(p), rows 8-15 remainders
+        uint32_t pa[NT / 2][4];
 #pragma unroll
-        for (int c = 0; c < KPT; ++c) {
-            const float pv = sc[c] == -INFINITY ? 0.f : expf(sc[c] - mn);
-            ps[r][sub + c * TPR] = pv;
-            psum += pv;
+        for (int kk = 0; kk < NT / 2; ++kk) {
+            float p[4];
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float s_ = sc[2 * kk + h][e];
+                    const float pv = s_ == -INFINITY ? 0.f : expf(s_ - mn);
+                    p[2 * h + e] = pv;
+                    ps += pv;
+                }
+            const float h0 = bf16_round_f(p[0]), h1 = bf16_round_f(p[1]), h2 = bf16_round_f(p[2]), h3 = bf16_round_f(p[3]);
+            pa[kk][0] = pack_bf16x2(h0, h1);
+            pa[kk][1] = pack_bf16x2(p[0] - h0, p[1] - h1);
+            pa[kk][2] = pack_bf16x2(h2, h3);
+            pa[kk][3] = pack_bf16x2(p[2] - h2, p[3] - h3);
         }
-#pragma unroll
-        for (int w = 1; w < TPR; w <<= 1) psum += __shfl_xor_sync(0xffffffffu, psum, w);
-        l_run = l_run * alpha + psum;
+        ps += __shfl_xor_sync(0xffffffffu, ps, 1);
+        ps += __shfl_xor_sync(0xffffffffu, ps, 2);
+        l_run = l_run * alpha + ps;
         m_run = mn;
-        __syncwarp();
 #pragma unroll
-        for (int e = 0; e < DPT; ++e) {
-            float acc = o[e] * alpha;
-            for (int kk = 0; kk < PF_KT; ++kk) acc = fmaf(ps[r][kk], vs[kk][sub * DPT + e], acc);
-            o[e] = acc;
+        for (int n = 0; n < DT; ++n) {
+            o[n][0] *= alpha; o[n][1] *= alpha; o[n][2] *= alpha; o[n][3] *= alpha;
         }
+        // O += P V: V tiles read transposed (k = keys, n = dims)
+#pragma unroll
+        for (int kk = 0; kk < NT / 2; ++kk)
+#pragma unroll
+            for (int d2 = 0; d2 < DT / 2; ++d2) {
+                uint32_t v0, v1, v2, v3;
+                ldsm_x4_t(smem_u32(vs + (16 * kk + rr + ((mi & 1) << 3)) * RS + 16 * d2 + ((mi >> 1) << 3)), v0, v1, v2,
+                          v3);
+                mma_bf16(o[2 * d2], pa[kk], v0, v1);
+                mma_bf16(o[2 * d2 + 1], pa[kk], v2, v3);
+            }
     }
-    if (!row_live) return;
+    if (!live) return;
+    // O of row gq = its bf16-part row + its remainder row
     const float inv = 1.0f / l_run;   // the row's own position is always visible: l_run > 0
 #pragma unroll
-    for (int e = 0; e < DPT; ++e) put_hilo(hb, qd, tq, hq * HD + sub * DPT + e, o[e] * inv);
+    for (int n = 0; n < DT; ++n)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) put_hilo(hb, qd, tok, head * HD + 8 * n + 2 * tq + e, (o[n][e] + o[n][2 + e]) * inv);
 }
 
 // SwiGLU of the gate/up splits: a = silu(gate) * up, as the down projection's hi/lo rows
@@ -225,6 +286,7 @@ __global__ void k_pf_swiglu(const float* part, int splits, int F, int nt, __nv_b
         float a = 0.f;
         if (t < nt) {
             float gs = 0.f, us = 0.f;
+#pragma unroll 4
             for (int s = 0; s < splits; ++s) {
                 const float* pr = part + ((size_t)s * PF_T + t) * 2 * F;
                 gs += pr[f];
@@ -418,11 +480,11 @@ static cudaError_t pf_gemm_launch(const PfProj& pr, cudaStream_t st) {
 
 static const void* pf_attn_fn(int hd, int G) {
     if (hd == 128) {
-        if (G == 4) return (const void*)&k_pf_attn<128, 4>;
-        if (G == 2) return (const void*)&k_pf_attn<128, 2>;
+        if (G == 4) return (const void*)&k_pf_attn_mma<128, 4>;
+        if (G == 2) return (const void*)&k_pf_attn_mma<128, 2>;
     } else if (hd == 64) {
-        if (G == 4) return (const void*)&k_pf_attn<64, 4>;
-        if (G == 2) return (const void*)&k_pf_attn<64, 2>;
+        if (G == 4) return (const void*)&k_pf_attn_mma<64, 4>;
+        if (G == 2) return (const void*)&k_pf_attn_mma<64, 2>;
     }
     return nullptr;
 }
@@ -456,7 +518,8 @@ cudaError_t prefill_run(PrefillState* s, const int* tokens, int n, int pos0, int
             {
                 void* args[] = {&s->q, const_cast<int*>(&a.Hq), const_cast<int*>(&nt), const_cast<int*>(&p0),
                                 const_cast<float*>(&scale), &kv, &s->hb};
-                if ((e = cudaLaunchKernel(attn, dim3((nt + PF_QB - 1) / PF_QB, a.Hkv), dim3(PF_AT), args, 0, st)) !=
+                const int tpc = PF_QR / G;   // tokens per attention CTA
+                if ((e = cudaLaunchKernel(attn, dim3((nt + tpc - 1) / tpc, a.Hkv), dim3(256), args, 0, st)) !=
                     cudaSuccess)
                     return e;
             }
