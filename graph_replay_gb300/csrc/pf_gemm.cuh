@@ -1,6 +1,6 @@
 // pf_gemm.cuh -- the prefill projections on the 5th-generation tensor cores
-// (tcgen05.mma, sm_103a): out[t, n] = sum_k W[n, k] * h[t, k] for a block of
-// PF_T tokens, W bf16 row-major [N, K] (nn.Linear layout), h fp32.
+// (tcgen05.mma, sm_103a): out[t, n] = sum_k W[n, k] * h[t, k] for the tokens
+// of a pass (blocks of PF_T), W bf16 row-major [N, K] (nn.Linear layout), h fp32.
 //
 // A prefill step is a dense contraction: at 128 tokens every weight byte feeds
 // 256 multiply-adds ("Models, Registry and the Driver", "The Model": a step
@@ -8,9 +8,11 @@
 // token, hi = bf16(h) and lo = bf16(h - hi), so the product keeps about 16
 // significant bits of h with fp32 accumulation; the weights are exact in bf16.
 //
-// One CTA computes a 128-row tile of W against all PF_T tokens over one K
-// split (up to three weight segments, e.g. Wq | Wk | Wv, share one launch and
-// one output row space): A = the W tile [128 x 64] and B = the activations [2 PF_T x 64] (hi
+// One CTA computes a 128-row tile of W against one block of PF_T tokens over
+// one K split (up to three weight segments, e.g. Wq | Wk | Wv, share one launch
+// and one output row space).  The token blocks are the grid's fastest index, so
+// the CTAs that share a weight tile run together and read it from HBM once.
+// A = the W tile [128 x 64] and B = the block's activations [2 PF_T x 64] (hi
 // rows, then lo rows) are staged by TMA (128-byte swizzle) in a ring of
 // PF_STAGES; one thread issues tcgen05.mma (kind::f16, bf16 x bf16 -> fp32)
 // into a TMEM accumulator of 128 lanes x 2 PF_T columns; each MMA group's
@@ -27,23 +29,25 @@ namespace gd {
 constexpr int PF_T = 128;                        // tokens per block
 constexpr int PF_BN = 2 * PF_T;                  // MMA N: hi rows, then lo rows
 constexpr int PF_BK = 64;                        // K per stage: one 128-byte swizzle atom of bf16
-constexpr int PF_STAGES = 4;
+constexpr int PF_STAGES = 2;                     // two CTAs per SM: one's epilogue overlaps the other's MMAs
 constexpr int PF_A_BYTES = 128 * PF_BK * 2;      // W tile
 constexpr int PF_B_BYTES = PF_BN * PF_BK * 2;    // activation tile
 constexpr int PF_STAGE = PF_A_BYTES + PF_B_BYTES;
 constexpr int PF_THREADS = 128;
 constexpr int PF_SMEM = PF_STAGES * PF_STAGE + 1024;
+constexpr int PF_CTAS_PER_SM = 2;                // TMEM: 2 x PF_BN = 512 columns
 
 struct PfGemmParams {
     CUtensorMap map_w[3];   // segment s: [rows_s, K] bf16, box [PF_BK, 128], 128-byte swizzle
-    CUtensorMap map_h;      // [PF_BN, K] bf16, box [PF_BK, PF_BN], 128-byte swizzle
+    CUtensorMap map_h;      // [blocks * PF_BN, K] bf16, box [PF_BK, PF_BN], 128-byte swizzle
     int tile0[4];           // first 128-row tile of each segment; tile0[nseg] = all tiles
     int row0[3];            // first output row of each segment
     int rows[3];            // rows of each segment
     int nseg;
-    float* part;            // [splits][PF_T][N] fp32
+    float* part;            // [splits][ntp][N] fp32
     int N;                  // output rows of all segments
     int ksteps;             // K steps of PF_BK per split
+    int ntp;                // token rows of a split's partial (blocks * PF_T)
     unsigned* err;          // FAULT_WAIT if a bounded wait gives up
 };
 
@@ -83,8 +87,8 @@ __device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t (&r)[32]) {
         : "r"(taddr));
 }
 
-// grid (tile0[nseg], splits), PF_THREADS threads, PF_SMEM dynamic shared memory
-__global__ void __launch_bounds__(PF_THREADS, 1) k_pf_gemm(const __grid_constant__ PfGemmParams p) {
+// grid (token blocks, tile0[nseg], splits), PF_THREADS threads, PF_SMEM dynamic shared memory
+__global__ void __launch_bounds__(PF_THREADS, PF_CTAS_PER_SM) k_pf_gemm(const __grid_constant__ PfGemmParams p) {
     extern __shared__ __align__(1024) unsigned char pf_raw[];
     unsigned char* ring =
         reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(pf_raw) + 1023) & ~(uintptr_t)1023);
@@ -92,11 +96,11 @@ __global__ void __launch_bounds__(PF_THREADS, 1) k_pf_gemm(const __grid_constant
     __shared__ uint32_t tmem;
     __shared__ int aborted;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int split = blockIdx.y;
+    const int blk = blockIdx.x, tile = blockIdx.y, split = blockIdx.z;
     // the weight segment of this tile
     int sg = 0;
-    while (sg + 1 < p.nseg && (int)blockIdx.x >= p.tile0[sg + 1]) ++sg;
-    const int mt = (int)blockIdx.x - p.tile0[sg];   // tile within the segment
+    while (sg + 1 < p.nseg && tile >= p.tile0[sg + 1]) ++sg;
+    const int mt = tile - p.tile0[sg];   // tile within the segment
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem)),
                      "n"(PF_BN)
@@ -133,7 +137,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) k_pf_gemm(const __grid_constant
                 const int k0 = (split * p.ksteps + ks) * PF_BK;
                 mbar_arrive_expect_tx(&full[s], PF_STAGE);
                 tma_load_2d(a, &p.map_w[sg], k0, mt * 128, &full[s]);
-                tma_load_2d(a + PF_A_BYTES, &p.map_h, k0, 0, &full[s]);
+                tma_load_2d(a + PF_A_BYTES, &p.map_h, k0, blk * PF_BN, &full[s]);
                 issued = ks + 1;
             }
         }
@@ -169,7 +173,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) k_pf_gemm(const __grid_constant
     const int n = p.row0[sg] + rs;
     if (ok && !*ab) {
         const uint32_t lanebase = dt + ((uint32_t)(warp * 32) << 16);
-        float* out = p.part + (size_t)split * PF_T * p.N;
+        float* out = p.part + ((size_t)split * p.ntp + (size_t)blk * PF_T) * p.N;
         for (int c = 0; c < PF_T; c += 32) {
             uint32_t hi[32], lo[32];
             tmem_ld_x32(lanebase + (uint32_t)c, hi);

@@ -2,15 +2,18 @@
 // Driver", "The Model": a step shape is rows x new tokens, positions are
 // absolute, so a prefill is a step continuing from a position).
 //
-// The prompt runs in blocks of PF_T = 128 tokens.  Per block and layer:
+// The prompt runs in passes of up to PF_PASS tokens (blocks of PF_T = 128 for
+// the tensor cores), layer by layer, so each pass reads every weight once.
+// Per pass and layer:
 //   RMSNorm -> QKV projection (tensor cores, pf_gemm.cuh) -> RoPE, K/V written
 //   into the sequence's store -> causal attention over every position up to
 //   each token (flash-style online softmax) -> O projection + residual ->
 //   RMSNorm -> gate/up projection -> SwiGLU -> down projection + residual.
-// After the last block the final token's hidden state goes through the
-// decoder's own head (final RMSNorm, LM head, greedy argmax).  Projections
-// split K over CTAs; the kernel that consumes a projection adds its splits in
-// split order, so results do not depend on scheduling.
+// After the last pass the final token's hidden state goes through the
+// decoder's own head (final RMSNorm, LM head, greedy argmax).  A projection
+// splits K over CTAs only when its tiles x token blocks do not fill the GPU;
+// the kernel that consumes a projection adds its splits in split order, so
+// results do not depend on scheduling.
 //
 // Activations enter the tensor cores as bf16 hi + lo rows (about 16
 // significant bits, fp32 accumulation); everything else is fp32, and K/V are
@@ -28,13 +31,31 @@ namespace gd {
 
 namespace {
 
-constexpr int PF_NT = 1024;        // threads of the per-token kernels
+constexpr int PF_NB = 8;                 // token blocks per pass
+constexpr int PF_PASS = PF_NB * PF_T;    // tokens per pass
+constexpr int PF_NT = 256;               // threads of the per-token kernels
 
-// hi / lo bf16 rows of one activation value (row t of the block and row PF_T + t)
+// hi / lo bf16 rows of one activation value: token t of the pass is row t % PF_T
+// of block t / PF_T, whose PF_BN rows are the block's hi rows, then its lo rows
+__device__ __forceinline__ size_t hilo_row(int t) { return (size_t)(t / PF_T) * PF_BN + (t % PF_T); }
 __device__ __forceinline__ void put_hilo(__nv_bfloat16* hb, int K, int t, int k, float v) {
     const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-    hb[(size_t)t * K + k] = hi;
-    hb[(size_t)(PF_T + t) * K + k] = __float2bfloat16_rn(v - __bfloat162float(hi));
+    const size_t r = hilo_row(t);
+    hb[r * K + k] = hi;
+    hb[(r + PF_T) * K + k] = __float2bfloat16_rn(v - __bfloat162float(hi));
+}
+// four consecutive values (k a multiple of 4)
+__device__ __forceinline__ void put_hilo4(__nv_bfloat16* hb, int K, int t, int k, float4 v) {
+    const float a[4] = {v.x, v.y, v.z, v.w};
+    float h[4], l[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        h[i] = bf16_round_f(a[i]);
+        l[i] = a[i] - h[i];
+    }
+    const size_t r = hilo_row(t);
+    *reinterpret_cast<uint2*>(hb + r * K + k) = make_uint2(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]));
+    *reinterpret_cast<uint2*>(hb + (r + PF_T) * K + k) = make_uint2(pack_bf16x2(l[0], l[1]), pack_bf16x2(l[2], l[3]));
 }
 
 __device__ __forceinline__ float block_sum(float v, float* red) {
@@ -48,36 +69,51 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
     return t;
 }
 
-// x[t] = E[tok[t]] (fp32) for the block's tokens; rows past nt are zero
+// x[t] = E[tok[t]] (fp32) for the pass's tokens; rows past nt are zero.  One
+// CTA per token row, 8 values per thread and step.
 __global__ void k_pf_embed(const __nv_bfloat16* E, const int* tok, int nt, int d, float* x) {
     const int t = blockIdx.x;
-    for (int i = threadIdx.x; i < d; i += blockDim.x)
-        x[(size_t)t * d + i] = t < nt ? __bfloat162float(E[(size_t)tok[t] * d + i]) : 0.f;
+    for (int i = threadIdx.x * 8; i < d; i += blockDim.x * 8) {
+        float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (t < nt) Elem<__nv_bfloat16>::unpack(*reinterpret_cast<const uint4*>(E + (size_t)tok[t] * d + i), f);
+        float4* o = reinterpret_cast<float4*>(x + (size_t)t * d + i);
+        o[0] = make_float4(f[0], f[1], f[2], f[3]);
+        o[1] = make_float4(f[4], f[5], f[6], f[7]);
+    }
 }
 
-// x[t] += sum over splits of part[s][t] (when part is given); then, when gain
-// is given, hb = hi/lo of x[t] / sqrt(mean(x[t]^2) + eps) * gain.  Rows past nt
-// give zero hb rows.  One CTA per token row of the block.
-__global__ void k_pf_resid_norm(float* x, const float* part, int splits, int d, const __nv_bfloat16* gain, float eps,
-                                int nt, __nv_bfloat16* hb) {
+// x[t] += sum over splits of part[s][t] (when part is given; ntp token rows per
+// split); then, when gain is given, hb = hi/lo of x[t] / sqrt(mean(x[t]^2) +
+// eps) * gain.  Rows past nt give zero hb rows.  One CTA per token row.
+__global__ void k_pf_resid_norm(float* x, const float* part, int splits, int ntp, int d, const __nv_bfloat16* gain,
+                                float eps, int nt, __nv_bfloat16* hb) {
     __shared__ float red[PF_NT / 32];
     const int t = blockIdx.x;
     float* xr = x + (size_t)t * d;
     float ss = 0.f;
-    for (int i = threadIdx.x; i < d; i += blockDim.x) {
-        float v = xr[i];
+    for (int i = threadIdx.x * 4; i < d; i += blockDim.x * 4) {
+        float4 v = *reinterpret_cast<const float4*>(xr + i);
         if (part && t < nt) {
-#pragma unroll 4
-            for (int s = 0; s < splits; ++s) v += part[((size_t)s * PF_T + t) * d + i];
-            xr[i] = v;
+            for (int s = 0; s < splits; ++s) {
+                const float4 p = *reinterpret_cast<const float4*>(part + ((size_t)s * ntp + t) * d + i);
+                v.x += p.x; v.y += p.y; v.z += p.z; v.w += p.w;
+            }
+            *reinterpret_cast<float4*>(xr + i) = v;
         }
-        ss = fmaf(v, v, ss);
+        ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
     }
     if (!gain) return;
     const float tot = block_sum(ss, red);
     const float inv = 1.0f / sqrtf(tot / (float)d + eps);
-    for (int i = threadIdx.x; i < d; i += blockDim.x)
-        put_hilo(hb, d, t, i, t < nt ? xr[i] * inv * __bfloat162float(gain[i]) : 0.f);
+    for (int i = threadIdx.x * 4; i < d; i += blockDim.x * 4) {
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (t < nt) {
+            const float4 xv = *reinterpret_cast<const float4*>(xr + i);
+            v = make_float4(xv.x * inv * __bfloat162float(gain[i]), xv.y * inv * __bfloat162float(gain[i + 1]),
+                            xv.z * inv * __bfloat162float(gain[i + 2]), xv.w * inv * __bfloat162float(gain[i + 3]));
+        }
+        put_hilo4(hb, d, t, i, v);
+    }
 }
 
 // the QKV splits of each token: RoPE of q and k at the token's position; q to
@@ -95,8 +131,8 @@ __device__ __forceinline__ size_t kv_off(const PfKv& kv, int g, int pos) {
     }
     return (((size_t)kv.row * kv.Hkv + g) * kv.cap + pos) * kv.hd;
 }
-__global__ void k_pf_qkv(const float* part, int splits, int Hq, int nt, int pos0, const float2* rope, float* qout,
-                         PfKv kv) {
+__global__ void k_pf_qkv(const float* part, int splits, int ntp, int Hq, int nt, int pos0, const float2* rope,
+                         float* qout, PfKv kv) {
     const int t = blockIdx.x;
     if (t >= nt) return;
     const int hd = kv.hd, h2 = hd / 2, qd = Hq * hd, kvd = kv.Hkv * hd, N = qd + 2 * kvd;
@@ -105,7 +141,7 @@ __global__ void k_pf_qkv(const float* part, int splits, int Hq, int nt, int pos0
     auto val = [&](int n) {
         float v = 0.f;
 #pragma unroll 4
-        for (int s = 0; s < splits; ++s) v += part[((size_t)s * PF_T + t) * N + n];
+        for (int s = 0; s < splits; ++s) v += part[((size_t)s * ntp + t) * N + n];
         return v;
     };
     for (int i = threadIdx.x; i < (Hq + kv.Hkv) * h2; i += blockDim.x) {   // q and k pairs
@@ -130,10 +166,22 @@ __global__ void k_pf_qkv(const float* part, int splits, int Hq, int nt, int pos0
     }
 }
 
+// 16-byte asynchronous copy global -> shared; zero bytes read (the 16 bytes
+// zero-filled) when !valid
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// every copy group of this thread but the newest has landed
+__device__ __forceinline__ void cp_async_wait_prev() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
 // Causal attention on the tensor cores (mma.sync m16n8k16, bf16 in, fp32
 // accumulate), flash-style.  A CTA takes 64 query rows -- PF_QR / G tokens x
 // the G query heads of kv head g, row r = token * G + head -- and sweeps the
-// keys [0, last position of its tokens] in tiles of PF_KT2 keys.  Warp w owns
+// keys [0, last position of its tokens] in tiles of PF_KT2 keys, double
+// buffered: the next tile's asynchronous copies are in flight while the
+// current one is computed.  The CTAs with the most keys start first.  Warp w owns
 // query rows 8w..8w+7: the MMA's 16 A rows hold their bf16 parts (rows 0-7) and
 // remainders (rows 8-15), so q keeps about 16 significant bits; S = Q K^T comes
 // out as hi + lo row pairs, and P (online softmax, fp32) goes back into the
@@ -143,6 +191,8 @@ __global__ void k_pf_qkv(const float* part, int splits, int Hq, int nt, int pos0
 // hi/lo activation rows.
 constexpr int PF_QR = 64;          // query rows per CTA
 constexpr int PF_KT2 = 64;         // keys per tile
+// dynamic shared memory of the attention kernel: two K and two V tiles
+__host__ __device__ constexpr int pf_attn_smem(int hd) { return 4 * PF_KT2 * (hd + 8) * 2; }
 template <int HD, int G>
 __global__ void __launch_bounds__(256) k_pf_attn_mma(const float* q, int Hq, int nt, int pos0, float scale, PfKv kv,
                                                      __nv_bfloat16* hb) {
@@ -151,9 +201,9 @@ __global__ void __launch_bounds__(256) k_pf_attn_mma(const float* q, int Hq, int
     constexpr int NT = PF_KT2 / 8;         // n-tiles of S
     constexpr int RS = HD + 8;             // shared row stride (bf16)
     constexpr int TPC = PF_QR / G;         // tokens per CTA
-    __shared__ __align__(16) __nv_bfloat16 ks[PF_KT2 * RS];
-    __shared__ __align__(16) __nv_bfloat16 vs[PF_KT2 * RS];
-    const int g = blockIdx.y, t0 = blockIdx.x * TPC, tid = threadIdx.x;
+    constexpr int TILE = PF_KT2 * RS;      // elements of one K (or V) tile
+    extern __shared__ __align__(16) __nv_bfloat16 pf_kv_smem[];   // K0, K1, V0, V1
+    const int g = blockIdx.y, t0 = (gridDim.x - 1 - blockIdx.x) * TPC, tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tq = lane & 3;
     const int qd = Hq * HD;
     // this lane's query row (warp row gq) and its position
@@ -184,21 +234,35 @@ __global__ void __launch_bounds__(256) k_pf_attn_mma(const float* q, int Hq, int
     float m_run = -INFINITY, l_run = 0.f;
     const int last = pos0 + min(t0 + TPC, nt) - 1;               // the last key any row of the CTA sees
     const int wlast = pos0 + min(t0 + (warp * 8 + 7) / G + 1, nt) - 1;   // ... any row of this warp
-    for (int j0 = 0; j0 <= last; j0 += PF_KT2) {
-        __syncthreads();
-        for (int i = tid; i < PF_KT2 * (HD / 8); i += 256) {     // 16-byte vectors of K and V
+    // copies of the tile at key j0 into buffer b (keys past `last` zero-filled)
+    auto load_tile = [&](int j0, int b) {
+        __nv_bfloat16* kd = pf_kv_smem + b * TILE;
+        __nv_bfloat16* vd = pf_kv_smem + (2 + b) * TILE;
+        for (int i = tid; i < PF_KT2 * (HD / 8); i += 256) {   // 16-byte vectors of K and V
             const int kk = i / (HD / 8), c = i % (HD / 8), j = j0 + kk;
-            uint4 kv4 = make_uint4(0u, 0u, 0u, 0u), vv4 = make_uint4(0u, 0u, 0u, 0u);
-            if (j <= last) {
-                const size_t off = kv_off(kv, g, j) + (size_t)c * 8;
-                kv4 = *reinterpret_cast<const uint4*>(kv.K + off);
-                vv4 = *reinterpret_cast<const uint4*>(kv.V + off);
-            }
-            *reinterpret_cast<uint4*>(ks + kk * RS + c * 8) = kv4;
-            *reinterpret_cast<uint4*>(vs + kk * RS + c * 8) = vv4;
+            const bool in = j <= last;
+            const size_t off = in ? kv_off(kv, g, j) + (size_t)c * 8 : 0;
+            cp_async16(kd + kk * RS + c * 8, kv.K + off, in);
+            cp_async16(vd + kk * RS + c * 8, kv.V + off, in);
         }
-        __syncthreads();
-        if (j0 > wlast) continue;   // every row of this warp is past these keys (masked)
+        cp_async_commit();
+    };
+    load_tile(0, 0);
+    int it = 0;
+    for (int j0 = 0; j0 <= last; j0 += PF_KT2, ++it) {
+        if (j0 + PF_KT2 <= last) {
+            load_tile(j0 + PF_KT2, (it + 1) & 1);
+        } else {
+            cp_async_commit();   // an empty group: the wait below still means "this tile has landed"
+        }
+        cp_async_wait_prev();
+        __syncthreads();   // every thread's copies of this tile are visible
+        const __nv_bfloat16* ks = pf_kv_smem + (it & 1) * TILE;
+        const __nv_bfloat16* vs = pf_kv_smem + (2 + (it & 1)) * TILE;
+        if (j0 > wlast) {   // every row of this warp is past these keys (masked)
+            __syncthreads();
+            continue;
+        }
         // S = Q K^T: 16 rows x PF_KT2 keys
         float sacc[NT][4];
 #pragma unroll
@@ -269,6 +333,7 @@ __global__ void __launch_bounds__(256) k_pf_attn_mma(const float* q, int Hq, int
                 mma_bf16(o[2 * d2], pa[kk], v0, v1);
                 mma_bf16(o[2 * d2 + 1], pa[kk], v2, v3);
             }
+        __syncthreads();   // this buffer is refilled by the next iteration's copies
     }
     if (!live) return;
     // O of row gq = its bf16-part row + its remainder row
@@ -279,33 +344,33 @@ __global__ void __launch_bounds__(256) k_pf_attn_mma(const float* q, int Hq, int
         for (int e = 0; e < 2; ++e) put_hilo(hb, qd, tok, head * HD + 8 * n + 2 * tq + e, (o[n][e] + o[n][2 + e]) * inv);
 }
 
-// SwiGLU of the gate/up splits: a = silu(gate) * up, as the down projection's hi/lo rows
-__global__ void k_pf_swiglu(const float* part, int splits, int F, int nt, __nv_bfloat16* hb) {
+// SwiGLU of the gate/up splits: a = silu(gate) * up, as the down projection's
+// hi/lo rows.  grid (token rows, F / (4 PF_NT)): four values per thread.
+__global__ void k_pf_swiglu(const float* part, int splits, int ntp, int F, int nt, __nv_bfloat16* hb) {
     const int t = blockIdx.x;
-    for (int f = threadIdx.x; f < F; f += blockDim.x) {
-        float a = 0.f;
-        if (t < nt) {
-            float gs = 0.f, us = 0.f;
-#pragma unroll 4
-            for (int s = 0; s < splits; ++s) {
-                const float* pr = part + ((size_t)s * PF_T + t) * 2 * F;
-                gs += pr[f];
-                us += pr[F + f];
-            }
-            a = gs / (1.0f + expf(-gs)) * us;
+    const int f = (blockIdx.y * blockDim.x + threadIdx.x) * 4;
+    if (f >= F) return;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (t < nt) {
+        float4 gs = a, us = a;
+        for (int s = 0; s < splits; ++s) {
+            const float* pr = part + ((size_t)s * ntp + t) * 2 * F;
+            const float4 gv = *reinterpret_cast<const float4*>(pr + f);
+            const float4 uv = *reinterpret_cast<const float4*>(pr + F + f);
+            gs.x += gv.x; gs.y += gv.y; gs.z += gv.z; gs.w += gv.w;
+            us.x += uv.x; us.y += uv.y; us.z += uv.z; us.w += uv.w;
         }
-        put_hilo(hb, F, t, f, a);
+        a = make_float4(gs.x / (1.0f + expf(-gs.x)) * us.x, gs.y / (1.0f + expf(-gs.y)) * us.y,
+                        gs.z / (1.0f + expf(-gs.z)) * us.z, gs.w / (1.0f + expf(-gs.w)) * us.w);
     }
+    put_hilo4(hb, F, t, f, a);
 }
 
-// rows of zeros for the hi/lo activation rows past the block's tokens (the
+// rows of zeros for the hi/lo activation rows past the pass's tokens (the
 // attention kernel writes only live rows)
 __global__ void k_pf_zero_rows(__nv_bfloat16* hb, int K, int nt) {
     const int t = nt + blockIdx.x;
-    for (int k = threadIdx.x; k < K; k += blockDim.x) {
-        hb[(size_t)t * K + k] = __float2bfloat16_rn(0.f);
-        hb[(size_t)(PF_T + t) * K + k] = __float2bfloat16_rn(0.f);
-    }
+    for (int k = threadIdx.x * 4; k < K; k += blockDim.x * 4) put_hilo4(hb, K, t, k, make_float4(0.f, 0.f, 0.f, 0.f));
 }
 
 typedef CUresult (*PfEncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -338,26 +403,39 @@ bool pf_map(CUtensorMap* m, const void* base, long long rows, long long cols, in
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// the fewest K splits (a divisor of the K steps, at most 16) that give at least
-// one CTA per SM
+// K splits (a divisor of the K steps, at most 16, at least 4 K steps each)
+// with the shortest modelled time: waves of the GPU's CTA slots x (K steps per
+// split + PF_CTA_COST, a CTA's fixed cost of pipeline fill and epilogue in K
+// steps).  More splits must win by a tenth: each adds a pass of partial sums
+// for the consuming kernel to read.
+constexpr int PF_CTA_COST = 6;
 int pf_splits(int tiles, int ksteps, int num_sms) {
-    for (int s = 1; s <= 16; ++s)
-        if (ksteps % s == 0 && tiles * s >= num_sms) return s;
-    for (int s = 16; s >= 1; --s)
-        if (ksteps % s == 0) return s;
-    return 1;
+    const int slots = num_sms * PF_CTAS_PER_SM;
+    int best = 1;
+    long long best_t = -1;
+    for (int s = 1; s <= 16; ++s) {
+        if (ksteps % s || (s > 1 && ksteps / s < 4)) continue;
+        const long long waves = ((long long)tiles * s + slots - 1) / slots;
+        const long long t = waves * (ksteps / s + PF_CTA_COST);
+        if (best_t < 0 || 10 * t < 9 * best_t) {
+            best_t = t;
+            best = s;
+        }
+    }
+    return best;
 }
 
 }  // namespace
 
-// one projection of the block: up to three stacked weight segments
+// one projection: up to three stacked weight segments
 struct PfProj {
     PfGemmParams p{};
-    int tiles = 0, splits = 1;
+    int tiles = 0, K = 0;
 };
 
 struct PrefillState {
     PrefillArgs a;
+    int num_sms = 0;
     float *x = nullptr, *part = nullptr, *q = nullptr;
     __nv_bfloat16* hb = nullptr;
     int* tok = nullptr;
@@ -366,14 +444,18 @@ struct PrefillState {
     size_t part_floats = 0;
 };
 
+// the partial-sum buffer: the largest splits x token rows x N over the
+// projections and the pass sizes (1..PF_NB blocks)
 size_t prefill_part_floats(const PrefillArgs& a, int num_sms) {
     const int qd = a.Hq * a.hd, kvd = a.Hkv * a.hd;
     size_t most = 0;
     auto need = [&](int N, int K) {
         const int tiles = (N + 127) / 128;
-        const int s = pf_splits(tiles, K / PF_BK, num_sms);
-        const size_t v = (size_t)s * PF_T * N;
-        if (v > most) most = v;
+        for (int nb = 1; nb <= PF_NB; ++nb) {
+            const int s = pf_splits(tiles * nb, K / PF_BK, num_sms);
+            const size_t v = (size_t)s * nb * PF_T * N;
+            if (v > most) most = v;
+        }
     };
     need(qd + 2 * kvd, a.d);
     need(a.d, qd);
@@ -402,18 +484,31 @@ void prefill_free(PrefillState* s) {
     delete s;
 }
 
+static const void* pf_attn_fn(int hd, int G) {
+    if (hd == 128) {
+        if (G == 4) return (const void*)&k_pf_attn_mma<128, 4>;
+        if (G == 2) return (const void*)&k_pf_attn_mma<128, 2>;
+    } else if (hd == 64) {
+        if (G == 4) return (const void*)&k_pf_attn_mma<64, 4>;
+        if (G == 2) return (const void*)&k_pf_attn_mma<64, 2>;
+    }
+    return nullptr;
+}
+
 cudaError_t prefill_create(const PrefillArgs& a, int num_sms, PrefillState** out) {
     *out = nullptr;
     PrefillState* s = new PrefillState();
     s->a = a;
+    s->num_sms = num_sms;
     const int qd = a.Hq * a.hd, kvd = a.Hkv * a.hd;
     const int kmax = a.d > qd ? (a.d > a.F ? a.d : a.F) : (qd > a.F ? qd : a.F);
     s->part_floats = prefill_part_floats(a, num_sms);
+    const long long hrows = (long long)PF_NB * PF_BN;   // hi/lo activation rows of a pass
     cudaError_t e;
-    if ((e = cudaMalloc(&s->x, sizeof(float) * PF_T * a.d)) != cudaSuccess ||
+    if ((e = cudaMalloc(&s->x, sizeof(float) * PF_PASS * a.d)) != cudaSuccess ||
         (e = cudaMalloc(&s->part, sizeof(float) * s->part_floats)) != cudaSuccess ||
-        (e = cudaMalloc(&s->q, sizeof(float) * PF_T * qd)) != cudaSuccess ||
-        (e = cudaMalloc(&s->hb, sizeof(__nv_bfloat16) * PF_BN * kmax)) != cudaSuccess ||
+        (e = cudaMalloc(&s->q, sizeof(float) * PF_PASS * qd)) != cudaSuccess ||
+        (e = cudaMalloc(&s->hb, sizeof(__nv_bfloat16) * hrows * kmax)) != cudaSuccess ||
         (e = cudaMalloc(&s->tok, sizeof(int) * a.cap)) != cudaSuccess ||
         (e = cudaMalloc(&s->pages, sizeof(int) * (a.paged ? a.ppr : 1))) != cudaSuccess) {
         cudaGetLastError();
@@ -422,8 +517,8 @@ cudaError_t prefill_create(const PrefillArgs& a, int num_sms, PrefillState** out
     }
     // tensor maps: every layer's weights, and the hi/lo activation rows for K = d, qd, F
     CUtensorMap hd_map, hq_map, hf_map;
-    if (!pf_map(&hd_map, s->hb, PF_BN, a.d, PF_BN) || !pf_map(&hq_map, s->hb, PF_BN, qd, PF_BN) ||
-        !pf_map(&hf_map, s->hb, PF_BN, a.F, PF_BN)) {
+    if (!pf_map(&hd_map, s->hb, hrows, a.d, PF_BN) || !pf_map(&hq_map, s->hb, hrows, qd, PF_BN) ||
+        !pf_map(&hf_map, s->hb, hrows, a.F, PF_BN)) {
         prefill_free(s);
         return cudaErrorInvalidValue;
     }
@@ -447,12 +542,11 @@ cudaError_t prefill_create(const PrefillArgs& a, int num_sms, PrefillState** out
         p.tile0[p.nseg] = tiles;
         p.map_h = hm;
         p.N = rows;
-        pr.tiles = tiles;
-        pr.splits = pf_splits(tiles, K / PF_BK, num_sms);
-        p.ksteps = K / PF_BK / pr.splits;
         p.part = s->part;
         p.err = a.err;
-        return (size_t)pr.splits * PF_T * rows <= s->part_floats;
+        pr.tiles = tiles;
+        pr.K = K;
+        return true;
     };
     s->proj.resize((size_t)a.L * 4);
     for (int l = 0; l < a.L; ++l) {
@@ -465,7 +559,9 @@ cudaError_t prefill_create(const PrefillArgs& a, int num_sms, PrefillState** out
             return cudaErrorInvalidValue;
         }
     }
-    if ((e = cudaFuncSetAttribute(k_pf_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, PF_SMEM)) != cudaSuccess) {
+    if ((e = cudaFuncSetAttribute(k_pf_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, PF_SMEM)) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(pf_attn_fn(a.hd, a.Hq / a.Hkv), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  pf_attn_smem(a.hd))) != cudaSuccess) {
         prefill_free(s);
         return e;
     }
@@ -473,20 +569,17 @@ cudaError_t prefill_create(const PrefillArgs& a, int num_sms, PrefillState** out
     return cudaSuccess;
 }
 
-static cudaError_t pf_gemm_launch(const PfProj& pr, cudaStream_t st) {
-    k_pf_gemm<<<dim3(pr.tiles, pr.splits), PF_THREADS, PF_SMEM, st>>>(pr.p);
+// one projection over nb token blocks; *splits gets its K splits
+static cudaError_t pf_gemm_launch(const PrefillState* s, const PfProj& pr, int nb, int* splits, cudaStream_t st) {
+    const int ks = pr.K / PF_BK;
+    const int sp = pf_splits(pr.tiles * nb, ks, s->num_sms);
+    PfGemmParams p = pr.p;
+    p.ksteps = ks / sp;
+    p.ntp = nb * PF_T;
+    if ((size_t)sp * p.ntp * p.N > s->part_floats) return cudaErrorInvalidValue;
+    *splits = sp;
+    k_pf_gemm<<<dim3(nb, pr.tiles, sp), PF_THREADS, PF_SMEM, st>>>(p);
     return cudaGetLastError();
-}
-
-static const void* pf_attn_fn(int hd, int G) {
-    if (hd == 128) {
-        if (G == 4) return (const void*)&k_pf_attn_mma<128, 4>;
-        if (G == 2) return (const void*)&k_pf_attn_mma<128, 2>;
-    } else if (hd == 64) {
-        if (G == 4) return (const void*)&k_pf_attn_mma<64, 4>;
-        if (G == 2) return (const void*)&k_pf_attn_mma<64, 2>;
-    }
-    return nullptr;
 }
 
 cudaError_t prefill_run(PrefillState* s, const int* tokens, int n, int pos0, int row, const int* pages,
@@ -501,43 +594,41 @@ cudaError_t prefill_run(PrefillState* s, const int* tokens, int n, int pos0, int
     const void* attn = pf_attn_fn(a.hd, G);
     if (!attn) return cudaErrorInvalidValue;
     const float scale = (float)(1.0 / sqrt((double)a.hd));
-    for (int c0 = 0; c0 < n; c0 += PF_T) {
-        const int nt = n - c0 < PF_T ? n - c0 : PF_T;
-        const int p0 = pos0 + c0;
-        k_pf_embed<<<PF_T, PF_NT, 0, st>>>(static_cast<const __nv_bfloat16*>(a.embed), s->tok + c0, nt, a.d, s->x);
-        k_pf_resid_norm<<<PF_T, PF_NT, 0, st>>>(s->x, nullptr, 0, a.d,
-                                                static_cast<const __nv_bfloat16*>(a.lw[0]), a.eps, nt, s->hb);
+    const dim3 swg(1, (a.F + 4 * PF_NT - 1) / (4 * PF_NT));
+    for (int c0 = 0; c0 < n; c0 += PF_PASS) {
+        int nt = n - c0 < PF_PASS ? n - c0 : PF_PASS;
+        const int nb = (nt + PF_T - 1) / PF_T, ntp = nb * PF_T;
+        int p0 = pos0 + c0;
+        k_pf_embed<<<ntp, PF_NT, 0, st>>>(static_cast<const __nv_bfloat16*>(a.embed), s->tok + c0, nt, a.d, s->x);
+        k_pf_resid_norm<<<ntp, PF_NT, 0, st>>>(s->x, nullptr, 0, ntp, a.d,
+                                               static_cast<const __nv_bfloat16*>(a.lw[0]), a.eps, nt, s->hb);
         for (int l = 0; l < a.L; ++l) {
             const void* const* w = a.lw + (size_t)l * 9;
             PfKv kv{static_cast<__nv_bfloat16*>(a.K[l]), static_cast<__nv_bfloat16*>(a.V[l]),
                     a.paged ? s->pages : nullptr, row, a.Hkv, a.hd, a.cap, a.page};
-            const PfProj& pq = s->proj[4 * l + 0];
-            if ((e = pf_gemm_launch(pq, st)) != cudaSuccess) return e;
-            k_pf_qkv<<<PF_T, PF_NT, 0, st>>>(s->part, pq.splits, a.Hq, nt, p0, a.rope, s->q, kv);
-            if (nt < PF_T) k_pf_zero_rows<<<PF_T - nt, PF_NT, 0, st>>>(s->hb, qd, nt);
+            int sp = 1;
+            if ((e = pf_gemm_launch(s, s->proj[4 * l + 0], nb, &sp, st)) != cudaSuccess) return e;
+            k_pf_qkv<<<nt, PF_NT, 0, st>>>(s->part, sp, ntp, a.Hq, nt, p0, a.rope, s->q, kv);
+            if (nt < ntp) k_pf_zero_rows<<<ntp - nt, PF_NT, 0, st>>>(s->hb, qd, nt);
             {
-                void* args[] = {&s->q, const_cast<int*>(&a.Hq), const_cast<int*>(&nt), const_cast<int*>(&p0),
-                                const_cast<float*>(&scale), &kv, &s->hb};
+                void* args[] = {&s->q, const_cast<int*>(&a.Hq), &nt, &p0, const_cast<float*>(&scale), &kv, &s->hb};
                 const int tpc = PF_QR / G;   // tokens per attention CTA
-                if ((e = cudaLaunchKernel(attn, dim3((nt + tpc - 1) / tpc, a.Hkv), dim3(256), args, 0, st)) !=
-                    cudaSuccess)
+                if ((e = cudaLaunchKernel(attn, dim3((nt + tpc - 1) / tpc, a.Hkv), dim3(256), args,
+                                          pf_attn_smem(a.hd), st)) != cudaSuccess)
                     return e;
             }
-            const PfProj& po = s->proj[4 * l + 1];
-            if ((e = pf_gemm_launch(po, st)) != cudaSuccess) return e;
-            k_pf_resid_norm<<<PF_T, PF_NT, 0, st>>>(s->x, s->part, po.splits, a.d,
-                                                    static_cast<const __nv_bfloat16*>(w[5]), a.eps, nt, s->hb);
-            const PfProj& pg = s->proj[4 * l + 2];
-            if ((e = pf_gemm_launch(pg, st)) != cudaSuccess) return e;
-            k_pf_swiglu<<<PF_T, PF_NT, 0, st>>>(s->part, pg.splits, a.F, nt, s->hb);
-            const PfProj& pd = s->proj[4 * l + 3];
-            if ((e = pf_gemm_launch(pd, st)) != cudaSuccess) return e;
+            if ((e = pf_gemm_launch(s, s->proj[4 * l + 1], nb, &sp, st)) != cudaSuccess) return e;
+            k_pf_resid_norm<<<ntp, PF_NT, 0, st>>>(s->x, s->part, sp, ntp, a.d,
+                                                   static_cast<const __nv_bfloat16*>(w[5]), a.eps, nt, s->hb);
+            if ((e = pf_gemm_launch(s, s->proj[4 * l + 2], nb, &sp, st)) != cudaSuccess) return e;
+            k_pf_swiglu<<<dim3(ntp, swg.y), PF_NT, 0, st>>>(s->part, sp, ntp, a.F, nt, s->hb);
+            if ((e = pf_gemm_launch(s, s->proj[4 * l + 3], nb, &sp, st)) != cudaSuccess) return e;
             const __nv_bfloat16* next_gain =
                 l + 1 < a.L ? static_cast<const __nv_bfloat16*>(a.lw[(size_t)(l + 1) * 9 + 0]) : nullptr;
-            k_pf_resid_norm<<<PF_T, PF_NT, 0, st>>>(s->x, s->part, pd.splits, a.d, next_gain, a.eps, nt, s->hb);
+            k_pf_resid_norm<<<ntp, PF_NT, 0, st>>>(s->x, s->part, sp, ntp, a.d, next_gain, a.eps, nt, s->hb);
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
         }
-        if (c0 + PF_T >= n &&
+        if (c0 + PF_PASS >= n &&
             (e = cudaMemcpyAsync(x_last, s->x + (size_t)(nt - 1) * a.d, sizeof(float) * a.d, cudaMemcpyDeviceToDevice,
                                  st)) != cudaSuccess)
             return e;
