@@ -17,8 +17,11 @@
 // PF_STAGES; one thread issues tcgen05.mma (kind::f16, bf16 x bf16 -> fp32)
 // into a TMEM accumulator of 128 lanes x 2 PF_T columns; each MMA group's
 // commit frees its ring stage.  The epilogue (all four warps, warp w reads TMEM
-// lanes 32w..32w+31) adds the hi and lo columns and stores the split's partial
-// sums part[split][t][n]; the caller adds the splits in split order.
+// lanes 32w..32w+31) adds the hi and lo columns and, by the launch's mode,
+// stores the split's partial sums part[split][t][n] (the caller adds the
+// splits in split order), adds the sums to the residual rows x[t][n] (one
+// split), or -- for a gate/up tile of 64 gate rows and the same 64 up rows --
+// writes silu(gate) * up as the down projection's hi/lo activation rows.
 #pragma once
 #include <cuda.h>
 #include "common.cuh"
@@ -37,6 +40,8 @@ constexpr int PF_THREADS = 128;
 constexpr int PF_SMEM = PF_STAGES * PF_STAGE + 1024;
 constexpr int PF_CTAS_PER_SM = 2;                // TMEM: 2 x PF_BN = 512 columns
 
+enum { PF_EPI_PART = 0, PF_EPI_ADD = 1, PF_EPI_SWIGLU = 2 };
+
 struct PfGemmParams {
     CUtensorMap map_w[3];   // segment s: [rows_s, K] bf16, box [PF_BK, 128], 128-byte swizzle
     CUtensorMap map_h;      // [blocks * PF_BN, K] bf16, box [PF_BK, PF_BN], 128-byte swizzle
@@ -48,6 +53,9 @@ struct PfGemmParams {
     int N;                  // output rows of all segments
     int ksteps;             // K steps of PF_BK per split
     int ntp;                // token rows of a split's partial (blocks * PF_T)
+    int mode;               // PF_EPI_*
+    float* x;               // PF_EPI_ADD: residual rows [ntp][N] (one split)
+    __nv_bfloat16* hb_out;  // PF_EPI_SWIGLU: hi/lo rows [blocks * PF_BN][N]; map_w[0] gate, map_w[1] up (64-row boxes)
     unsigned* err;          // FAULT_WAIT if a bounded wait gives up
 };
 
@@ -136,7 +144,12 @@ __global__ void __launch_bounds__(PF_THREADS, PF_CTAS_PER_SM) k_pf_gemm(const __
                 unsigned char* a = ring + (size_t)s * PF_STAGE;
                 const int k0 = (split * p.ksteps + ks) * PF_BK;
                 mbar_arrive_expect_tx(&full[s], PF_STAGE);
-                tma_load_2d(a, &p.map_w[sg], k0, mt * 128, &full[s]);
+                if (p.mode == PF_EPI_SWIGLU) {   // A rows 0-63: gate rows of the tile, 64-127: the same up rows
+                    tma_load_2d(a, &p.map_w[0], k0, tile * 64, &full[s]);
+                    tma_load_2d(a + PF_A_BYTES / 2, &p.map_w[1], k0, tile * 64, &full[s]);
+                } else {
+                    tma_load_2d(a, &p.map_w[sg], k0, mt * 128, &full[s]);
+                }
                 tma_load_2d(a + PF_A_BYTES, &p.map_h, k0, blk * PF_BN, &full[s]);
                 issued = ks + 1;
             }
@@ -171,19 +184,58 @@ __global__ void __launch_bounds__(PF_THREADS, PF_CTAS_PER_SM) k_pf_gemm(const __
     if (!ok) atomicOr(p.err, FAULT_WAIT);
     const int rs = mt * 128 + warp * 32 + lane;
     const int n = p.row0[sg] + rs;
-    if (ok && !*ab) {
-        const uint32_t lanebase = dt + ((uint32_t)(warp * 32) << 16);
-        float* out = p.part + ((size_t)split * p.ntp + (size_t)blk * PF_T) * p.N;
+    const uint32_t lanebase = dt + ((uint32_t)(warp * 32) << 16);
+    if (p.mode == PF_EPI_SWIGLU) {
+        // the gate rows' sums (TMEM lanes 0-63) and the up rows' sums (lanes
+        // 64-127) meet in shared memory -- the ring: every copy has landed and
+        // every MMA has read it -- and all four warps write silu(gate) * up
+        constexpr int US = PF_T + 1;   // padded row: the lanes of a column hit distinct banks
+        float* gu_s = reinterpret_cast<float*>(ring);   // [128 rows][US]
+        const bool live = ok && !*ab;
+        fence_proxy_async_smem();
+        if (live) {
+            for (int c = 0; c < PF_T; c += 32) {
+                uint32_t hi[32], lo[32];
+                tmem_ld_x32(lanebase + (uint32_t)c, hi);
+                tmem_ld_x32(lanebase + (uint32_t)(PF_T + c), lo);
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+                for (int t = 0; t < 32; ++t)
+                    gu_s[(warp * 32 + lane) * US + c + t] = __uint_as_float(hi[t]) + __uint_as_float(lo[t]);
+            }
+        }
+        __syncthreads();
+        if (live) {
+            // thread: row f = tid % 64 of the tile, tokens tid / 64 + 2 j
+            const int fr = tid & 63, t0 = tid >> 6;
+            __nv_bfloat16* hrow = p.hb_out + (size_t)blk * PF_BN * p.N + (size_t)tile * 64 + fr;
+#pragma unroll 4
+            for (int j = 0; j < PF_T / 2; ++j) {
+                const int t = t0 + 2 * j;
+                const float gs = gu_s[fr * US + t], us = gu_s[(64 + fr) * US + t];
+                const float a = gs / (1.0f + expf(-gs)) * us;
+                const __nv_bfloat16 ah = __float2bfloat16_rn(a);
+                hrow[(size_t)t * p.N] = ah;
+                hrow[(size_t)(PF_T + t) * p.N] = __float2bfloat16_rn(a - __bfloat162float(ah));
+            }
+        }
+    } else if (ok && !*ab) {
+        const bool add = p.mode == PF_EPI_ADD;
+        float* out = add ? p.x + (size_t)blk * PF_T * p.N : p.part + ((size_t)split * p.ntp + (size_t)blk * PF_T) * p.N;
         for (int c = 0; c < PF_T; c += 32) {
             uint32_t hi[32], lo[32];
             tmem_ld_x32(lanebase + (uint32_t)c, hi);
             tmem_ld_x32(lanebase + (uint32_t)(PF_T + c), lo);
+            const bool inrow = rs < p.rows[sg];
+            float xv[32];   // the residual values: every load in flight before any store
+#pragma unroll
+            for (int t = 0; t < 32; ++t) xv[t] = (add && inrow) ? out[(size_t)(c + t) * p.N + n] : 0.f;
             asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-            if (rs < p.rows[sg]) {
+            if (inrow) {
 #pragma unroll
                 for (int t = 0; t < 32; ++t) {
                     asm volatile("" : "+r"(hi[t]), "+r"(lo[t]));
-                    out[(size_t)(c + t) * p.N + n] = __uint_as_float(hi[t]) + __uint_as_float(lo[t]);
+                    out[(size_t)(c + t) * p.N + n] = xv[t] + (__uint_as_float(hi[t]) + __uint_as_float(lo[t]));
                 }
             }
         }

@@ -8,12 +8,14 @@
 //   RMSNorm -> QKV projection (tensor cores, pf_gemm.cuh) -> RoPE, K/V written
 //   into the sequence's store -> causal attention over every position up to
 //   each token (flash-style online softmax) -> O projection + residual ->
-//   RMSNorm -> gate/up projection -> SwiGLU -> down projection + residual.
+//   RMSNorm -> gate/up projection with SwiGLU in its epilogue -> down
+//   projection + residual.
 // After the last pass the final token's hidden state goes through the
 // decoder's own head (final RMSNorm, LM head, greedy argmax).  A projection
 // splits K over CTAs only when its tiles x token blocks do not fill the GPU;
 // the kernel that consumes a projection adds its splits in split order, so
-// results do not depend on scheduling.
+// results do not depend on scheduling.  Unsplit O and down projections add
+// into the residual rows in their own epilogue.
 //
 // Activations enter the tensor cores as bf16 hi + lo rows (about 16
 // significant bits, fp32 accumulation); everything else is fp32, and K/V are
@@ -95,7 +97,7 @@ __global__ void k_pf_resid_norm(float* x, const float* part, int splits, int ntp
         float4 v = *reinterpret_cast<const float4*>(xr + i);
         if (part && t < nt) {
             for (int s = 0; s < splits; ++s) {
-                const float4 p = *reinterpret_cast<const float4*>(part + ((size_t)s * ntp + t) * d + i);
+                const float4 p = __ldg(reinterpret_cast<const float4*>(part + ((size_t)s * ntp + t) * d + i));
                 v.x += p.x; v.y += p.y; v.z += p.z; v.w += p.w;
             }
             *reinterpret_cast<float4*>(xr + i) = v;
@@ -126,11 +128,13 @@ struct PfKv {
 };
 __device__ __forceinline__ size_t kv_off(const PfKv& kv, int g, int pos) {
     if (kv.pages) {
-        const int pg = kv.pages[pos / kv.page], o = pos % kv.page;
+        const int pg = __ldg(kv.pages + pos / kv.page), o = pos % kv.page;
         return (((size_t)pg * kv.Hkv + g) * kv.page + o) * kv.hd;
     }
     return (((size_t)kv.row * kv.Hkv + g) * kv.cap + pos) * kv.hd;
 }
+// (the partial sums, the RoPE table and the page table are read-only here:
+// non-coherent loads, free to move ahead of this kernel's stores)
 __global__ void k_pf_qkv(const float* part, int splits, int ntp, int Hq, int nt, int pos0, const float2* rope,
                          float* qout, PfKv kv) {
     const int t = blockIdx.x;
@@ -141,15 +145,16 @@ __global__ void k_pf_qkv(const float* part, int splits, int ntp, int Hq, int nt,
     auto val = [&](int n) {
         float v = 0.f;
 #pragma unroll 4
-        for (int s = 0; s < splits; ++s) v += part[((size_t)s * ntp + t) * N + n];
+        for (int s = 0; s < splits; ++s) v += __ldg(part + ((size_t)s * ntp + t) * N + n);
         return v;
     };
+#pragma unroll 2
     for (int i = threadIdx.x; i < (Hq + kv.Hkv) * h2; i += blockDim.x) {   // q and k pairs
         const int hh = i / h2, e = i % h2;
         const bool is_q = hh < Hq;
         const int base = is_q ? hh * hd : qd + (hh - Hq) * hd;
         const float a = val(base + e), b = val(base + e + h2);
-        const float2 cs = rt[e];
+        const float2 cs = __ldg(rt + e);
         const float r0 = a * cs.x - b * cs.y, r1 = a * cs.y + b * cs.x;
         if (is_q) {
             qout[(size_t)t * qd + hh * hd + e] = r0;
@@ -160,6 +165,7 @@ __global__ void k_pf_qkv(const float* part, int splits, int ntp, int Hq, int nt,
             kv.K[o + e + h2] = __float2bfloat16_rn(r1);
         }
     }
+#pragma unroll 2
     for (int i = threadIdx.x; i < kvd; i += blockDim.x) {   // v
         const int g = i / hd, e = i % hd;
         kv.V[kv_off(kv, g, pos) + e] = __float2bfloat16_rn(val(qd + kvd + i));
@@ -344,28 +350,6 @@ __global__ void __launch_bounds__(256) k_pf_attn_mma(const float* q, int Hq, int
         for (int e = 0; e < 2; ++e) put_hilo(hb, qd, tok, head * HD + 8 * n + 2 * tq + e, (o[n][e] + o[n][2 + e]) * inv);
 }
 
-// SwiGLU of the gate/up splits: a = silu(gate) * up, as the down projection's
-// hi/lo rows.  grid (token rows, F / (4 PF_NT)): four values per thread.
-__global__ void k_pf_swiglu(const float* part, int splits, int ntp, int F, int nt, __nv_bfloat16* hb) {
-    const int t = blockIdx.x;
-    const int f = (blockIdx.y * blockDim.x + threadIdx.x) * 4;
-    if (f >= F) return;
-    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (t < nt) {
-        float4 gs = a, us = a;
-        for (int s = 0; s < splits; ++s) {
-            const float* pr = part + ((size_t)s * ntp + t) * 2 * F;
-            const float4 gv = *reinterpret_cast<const float4*>(pr + f);
-            const float4 uv = *reinterpret_cast<const float4*>(pr + F + f);
-            gs.x += gv.x; gs.y += gv.y; gs.z += gv.z; gs.w += gv.w;
-            us.x += uv.x; us.y += uv.y; us.z += uv.z; us.w += uv.w;
-        }
-        a = make_float4(gs.x / (1.0f + expf(-gs.x)) * us.x, gs.y / (1.0f + expf(-gs.y)) * us.y,
-                        gs.z / (1.0f + expf(-gs.z)) * us.z, gs.w / (1.0f + expf(-gs.w)) * us.w);
-    }
-    put_hilo4(hb, F, t, f, a);
-}
-
 // rows of zeros for the hi/lo activation rows past the pass's tokens (the
 // attention kernel writes only live rows)
 __global__ void k_pf_zero_rows(__nv_bfloat16* hb, int K, int nt) {
@@ -431,13 +415,16 @@ int pf_splits(int tiles, int ksteps, int num_sms) {
 struct PfProj {
     PfGemmParams p{};
     int tiles = 0, K = 0;
+    bool add = false;      // O / down: unsplit launches add into the residual rows
+    bool swiglu = false;   // gate/up: never split, SwiGLU epilogue
 };
 
 struct PrefillState {
     PrefillArgs a;
     int num_sms = 0;
     float *x = nullptr, *part = nullptr, *q = nullptr;
-    __nv_bfloat16* hb = nullptr;
+    __nv_bfloat16* hb = nullptr;    // hi/lo rows of the projections with K = d or Hq hd
+    __nv_bfloat16* hb2 = nullptr;   // hi/lo rows of the down projection (K = F)
     int* tok = nullptr;
     int* pages = nullptr;
     std::vector<PfProj> proj;   // per layer: qkv, o, gate/up, down
@@ -459,7 +446,6 @@ size_t prefill_part_floats(const PrefillArgs& a, int num_sms) {
     };
     need(qd + 2 * kvd, a.d);
     need(a.d, qd);
-    need(2 * a.F, a.d);
     need(a.d, a.F);
     return most;
 }
@@ -479,6 +465,7 @@ void prefill_free(PrefillState* s) {
     cudaFree(s->part);
     cudaFree(s->q);
     cudaFree(s->hb);
+    cudaFree(s->hb2);
     cudaFree(s->tok);
     cudaFree(s->pages);
     delete s;
@@ -501,7 +488,7 @@ cudaError_t prefill_create(const PrefillArgs& a, int num_sms, PrefillState** out
     s->a = a;
     s->num_sms = num_sms;
     const int qd = a.Hq * a.hd, kvd = a.Hkv * a.hd;
-    const int kmax = a.d > qd ? (a.d > a.F ? a.d : a.F) : (qd > a.F ? qd : a.F);
+    const int kmax = a.d > qd ? a.d : qd;
     s->part_floats = prefill_part_floats(a, num_sms);
     const long long hrows = (long long)PF_NB * PF_BN;   // hi/lo activation rows of a pass
     cudaError_t e;
@@ -509,6 +496,7 @@ cudaError_t prefill_create(const PrefillArgs& a, int num_sms, PrefillState** out
         (e = cudaMalloc(&s->part, sizeof(float) * s->part_floats)) != cudaSuccess ||
         (e = cudaMalloc(&s->q, sizeof(float) * PF_PASS * qd)) != cudaSuccess ||
         (e = cudaMalloc(&s->hb, sizeof(__nv_bfloat16) * hrows * kmax)) != cudaSuccess ||
+        (e = cudaMalloc(&s->hb2, sizeof(__nv_bfloat16) * hrows * a.F)) != cudaSuccess ||
         (e = cudaMalloc(&s->tok, sizeof(int) * a.cap)) != cudaSuccess ||
         (e = cudaMalloc(&s->pages, sizeof(int) * (a.paged ? a.ppr : 1))) != cudaSuccess) {
         cudaGetLastError();
@@ -518,7 +506,7 @@ cudaError_t prefill_create(const PrefillArgs& a, int num_sms, PrefillState** out
     // tensor maps: every layer's weights, and the hi/lo activation rows for K = d, qd, F
     CUtensorMap hd_map, hq_map, hf_map;
     if (!pf_map(&hd_map, s->hb, hrows, a.d, PF_BN) || !pf_map(&hq_map, s->hb, hrows, qd, PF_BN) ||
-        !pf_map(&hf_map, s->hb, hrows, a.F, PF_BN)) {
+        !pf_map(&hf_map, s->hb2, hrows, a.F, PF_BN)) {
         prefill_free(s);
         return cudaErrorInvalidValue;
     }
@@ -543,9 +531,30 @@ cudaError_t prefill_create(const PrefillArgs& a, int num_sms, PrefillState** out
         p.map_h = hm;
         p.N = rows;
         p.part = s->part;
+        p.x = s->x;
         p.err = a.err;
         pr.tiles = tiles;
         pr.K = K;
+        return true;
+    };
+    // gate/up: tile i = gate rows [64 i, 64 i + 64) over the same up rows, written
+    // as silu(gate) * up into the down projection's hi/lo rows
+    auto proj_gu = [&](const void* wg, const void* wu, PfProj& pr) {
+        PfGemmParams& p = pr.p;
+        if (!pf_map(&p.map_w[0], wg, a.F, a.d, 64) || !pf_map(&p.map_w[1], wu, a.F, a.d, 64)) return false;
+        p.nseg = 1;
+        p.tile0[0] = 0;
+        p.tile0[1] = a.F / 64;
+        p.row0[0] = 0;
+        p.rows[0] = a.F;
+        p.map_h = hd_map;
+        p.N = a.F;
+        p.mode = PF_EPI_SWIGLU;
+        p.hb_out = s->hb2;
+        p.err = a.err;
+        pr.tiles = a.F / 64;
+        pr.K = a.d;
+        pr.swiglu = true;
         return true;
     };
     s->proj.resize((size_t)a.L * 4);
@@ -553,11 +562,13 @@ cudaError_t prefill_create(const PrefillArgs& a, int num_sms, PrefillState** out
         const void* const* w = a.lw + (size_t)l * 9;   // attn_norm, q, k, v, o, ffn_norm, gate, up, down
         if (!proj(w[1], qd, w[2], kvd, w[3], kvd, a.d, hd_map, s->proj[4 * l + 0]) ||
             !proj(w[4], a.d, nullptr, 0, nullptr, 0, qd, hq_map, s->proj[4 * l + 1]) ||
-            !proj(w[6], a.F, w[7], a.F, nullptr, 0, a.d, hd_map, s->proj[4 * l + 2]) ||
+            !proj_gu(w[6], w[7], s->proj[4 * l + 2]) ||
             !proj(w[8], a.d, nullptr, 0, nullptr, 0, a.F, hf_map, s->proj[4 * l + 3])) {
             prefill_free(s);
             return cudaErrorInvalidValue;
         }
+        s->proj[4 * l + 1].add = true;
+        s->proj[4 * l + 3].add = true;
     }
     if ((e = cudaFuncSetAttribute(k_pf_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, PF_SMEM)) != cudaSuccess ||
         (e = cudaFuncSetAttribute(pf_attn_fn(a.hd, a.Hq / a.Hkv), cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -569,15 +580,17 @@ cudaError_t prefill_create(const PrefillArgs& a, int num_sms, PrefillState** out
     return cudaSuccess;
 }
 
-// one projection over nb token blocks; *splits gets its K splits
+// one projection over nb token blocks; *splits gets its K splits (0: the
+// epilogue added into the residual rows or wrote SwiGLU, nothing to add up)
 static cudaError_t pf_gemm_launch(const PrefillState* s, const PfProj& pr, int nb, int* splits, cudaStream_t st) {
     const int ks = pr.K / PF_BK;
-    const int sp = pf_splits(pr.tiles * nb, ks, s->num_sms);
+    const int sp = pr.swiglu ? 1 : pf_splits(pr.tiles * nb, ks, s->num_sms);
     PfGemmParams p = pr.p;
     p.ksteps = ks / sp;
     p.ntp = nb * PF_T;
-    if ((size_t)sp * p.ntp * p.N > s->part_floats) return cudaErrorInvalidValue;
-    *splits = sp;
+    if (!pr.swiglu) p.mode = (pr.add && sp == 1) ? PF_EPI_ADD : PF_EPI_PART;
+    if (p.mode == PF_EPI_PART && (size_t)sp * p.ntp * p.N > s->part_floats) return cudaErrorInvalidValue;
+    *splits = p.mode == PF_EPI_PART ? sp : 0;
     k_pf_gemm<<<dim3(nb, pr.tiles, sp), PF_THREADS, PF_SMEM, st>>>(p);
     return cudaGetLastError();
 }
@@ -594,7 +607,6 @@ cudaError_t prefill_run(PrefillState* s, const int* tokens, int n, int pos0, int
     const void* attn = pf_attn_fn(a.hd, G);
     if (!attn) return cudaErrorInvalidValue;
     const float scale = (float)(1.0 / sqrt((double)a.hd));
-    const dim3 swg(1, (a.F + 4 * PF_NT - 1) / (4 * PF_NT));
     for (int c0 = 0; c0 < n; c0 += PF_PASS) {
         int nt = n - c0 < PF_PASS ? n - c0 : PF_PASS;
         const int nb = (nt + PF_T - 1) / PF_T, ntp = nb * PF_T;
@@ -618,14 +630,15 @@ cudaError_t prefill_run(PrefillState* s, const int* tokens, int n, int pos0, int
                     return e;
             }
             if ((e = pf_gemm_launch(s, s->proj[4 * l + 1], nb, &sp, st)) != cudaSuccess) return e;
-            k_pf_resid_norm<<<ntp, PF_NT, 0, st>>>(s->x, s->part, sp, ntp, a.d,
+            k_pf_resid_norm<<<ntp, PF_NT, 0, st>>>(s->x, sp ? s->part : nullptr, sp, ntp, a.d,
                                                    static_cast<const __nv_bfloat16*>(w[5]), a.eps, nt, s->hb);
             if ((e = pf_gemm_launch(s, s->proj[4 * l + 2], nb, &sp, st)) != cudaSuccess) return e;
-            k_pf_swiglu<<<dim3(ntp, swg.y), PF_NT, 0, st>>>(s->part, sp, ntp, a.F, nt, s->hb);
             if ((e = pf_gemm_launch(s, s->proj[4 * l + 3], nb, &sp, st)) != cudaSuccess) return e;
             const __nv_bfloat16* next_gain =
                 l + 1 < a.L ? static_cast<const __nv_bfloat16*>(a.lw[(size_t)(l + 1) * 9 + 0]) : nullptr;
-            k_pf_resid_norm<<<ntp, PF_NT, 0, st>>>(s->x, s->part, sp, ntp, a.d, next_gain, a.eps, nt, s->hb);
+            if (sp || next_gain)
+                k_pf_resid_norm<<<ntp, PF_NT, 0, st>>>(s->x, sp ? s->part : nullptr, sp, ntp, a.d, next_gain, a.eps,
+                                                       nt, s->hb);
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
         }
         if (c0 + PF_PASS >= n &&
