@@ -133,8 +133,12 @@ __device__ __forceinline__ size_t kv_off(const PfKv& kv, int g, int pos) {
     }
     return (((size_t)kv.row * kv.Hkv + g) * kv.cap + pos) * kv.hd;
 }
-// (the partial sums, the RoPE table and the page table are read-only here:
-// non-coherent loads, free to move ahead of this kernel's stores)
+// Four consecutive dims per thread and step (16-byte loads), every load of a
+// step issued before its arithmetic; the partial sums, the RoPE table and the
+// page table are read-only here (non-coherent loads).
+__device__ __forceinline__ float4 f4add(float4 a, float4 b) {
+    return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+}
 __global__ void k_pf_qkv(const float* part, int splits, int ntp, int Hq, int nt, int pos0, const float2* rope,
                          float* qout, PfKv kv) {
     const int t = blockIdx.x;
@@ -142,33 +146,49 @@ __global__ void k_pf_qkv(const float* part, int splits, int ntp, int Hq, int nt,
     const int hd = kv.hd, h2 = hd / 2, qd = Hq * hd, kvd = kv.Hkv * hd, N = qd + 2 * kvd;
     const int pos = pos0 + t;
     const float2* rt = rope + (size_t)pos * h2;
-    auto val = [&](int n) {
-        float v = 0.f;
-#pragma unroll 4
-        for (int s = 0; s < splits; ++s) v += __ldg(part + ((size_t)s * ntp + t) * N + n);
-        return v;
-    };
-#pragma unroll 2
-    for (int i = threadIdx.x; i < (Hq + kv.Hkv) * h2; i += blockDim.x) {   // q and k pairs
-        const int hh = i / h2, e = i % h2;
-        const bool is_q = hh < Hq;
-        const int base = is_q ? hh * hd : qd + (hh - Hq) * hd;
-        const float a = val(base + e), b = val(base + e + h2);
-        const float2 cs = __ldg(rt + e);
-        const float r0 = a * cs.x - b * cs.y, r1 = a * cs.y + b * cs.x;
-        if (is_q) {
-            qout[(size_t)t * qd + hh * hd + e] = r0;
-            qout[(size_t)t * qd + hh * hd + e + h2] = r1;
+    const int q4 = h2 / 4;                          // 4-dim groups per half head
+    const int npair = (Hq + kv.Hkv) * q4;           // q and k: (head, group) pairs
+    const int nv = kvd / 4;                         // v: 4-dim groups
+    for (int i = threadIdx.x; i < npair + nv; i += blockDim.x) {
+        const float* pp = part + (size_t)t * N;
+        if (i < npair) {
+            const int hh = i / q4, e = (i % q4) * 4;
+            const bool is_q = hh < Hq;
+            const int base = is_q ? hh * hd : qd + (hh - Hq) * hd;
+            float4 a = __ldg(reinterpret_cast<const float4*>(pp + base + e));
+            float4 b = __ldg(reinterpret_cast<const float4*>(pp + base + e + h2));
+            for (int s = 1; s < splits; ++s) {
+                const float* ps = pp + (size_t)s * ntp * N;
+                a = f4add(a, __ldg(reinterpret_cast<const float4*>(ps + base + e)));
+                b = f4add(b, __ldg(reinterpret_cast<const float4*>(ps + base + e + h2)));
+            }
+            const float4 c01 = __ldg(reinterpret_cast<const float4*>(rt + e));       // (cos, sin) of e, e + 1
+            const float4 c23 = __ldg(reinterpret_cast<const float4*>(rt + e + 2));   // ... of e + 2, e + 3
+            const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+            const float cs[4] = {c01.x, c01.z, c23.x, c23.z}, sn[4] = {c01.y, c01.w, c23.y, c23.w};
+            float r0[4], r1[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                r0[j] = av[j] * cs[j] - bv[j] * sn[j];
+                r1[j] = av[j] * sn[j] + bv[j] * cs[j];
+            }
+            if (is_q) {
+                float* qo = qout + (size_t)t * qd + hh * hd + e;
+                *reinterpret_cast<float4*>(qo) = make_float4(r0[0], r0[1], r0[2], r0[3]);
+                *reinterpret_cast<float4*>(qo + h2) = make_float4(r1[0], r1[1], r1[2], r1[3]);
+            } else {
+                __nv_bfloat16* ko = kv.K + kv_off(kv, hh - Hq, pos) + e;
+                *reinterpret_cast<uint2*>(ko) = make_uint2(pack_bf16x2(r0[0], r0[1]), pack_bf16x2(r0[2], r0[3]));
+                *reinterpret_cast<uint2*>(ko + h2) = make_uint2(pack_bf16x2(r1[0], r1[1]), pack_bf16x2(r1[2], r1[3]));
+            }
         } else {
-            const size_t o = kv_off(kv, hh - Hq, pos);
-            kv.K[o + e] = __float2bfloat16_rn(r0);
-            kv.K[o + e + h2] = __float2bfloat16_rn(r1);
+            const int j = (i - npair) * 4, g = j / hd, e = j % hd;
+            float4 v = __ldg(reinterpret_cast<const float4*>(pp + qd + kvd + j));
+            for (int s = 1; s < splits; ++s)
+                v = f4add(v, __ldg(reinterpret_cast<const float4*>(pp + (size_t)s * ntp * N + qd + kvd + j)));
+            *reinterpret_cast<uint2*>(kv.V + kv_off(kv, g, pos) + e) =
+                make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
         }
-    }
-#pragma unroll 2
-    for (int i = threadIdx.x; i < kvd; i += blockDim.x) {   // v
-        const int g = i / hd, e = i % hd;
-        kv.V[kv_off(kv, g, pos) + e] = __float2bfloat16_rn(val(qd + kvd + i));
     }
 }
 
