@@ -71,6 +71,14 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
     return t;
 }
 
+// two bf16 values (low half first) widened exactly to fp32
+__device__ __forceinline__ float2 bf16x2_to_f2(uint32_t u) {
+    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+}
+__device__ __forceinline__ float4 f4add(float4 a, float4 b) {
+    return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+}
+
 // x[t] = E[tok[t]] (fp32) for the pass's tokens; rows past nt are zero.  One
 // CTA per token row, 8 values per thread and step.
 __global__ void k_pf_embed(const __nv_bfloat16* E, const int* tok, int nt, int d, float* x) {
@@ -86,35 +94,48 @@ __global__ void k_pf_embed(const __nv_bfloat16* E, const int* tok, int nt, int d
 
 // x[t] += sum over splits of part[s][t] (when part is given; ntp token rows per
 // split); then, when gain is given, hb = hi/lo of x[t] / sqrt(mean(x[t]^2) +
-// eps) * gain.  Rows past nt give zero hb rows.  One CTA per token row.
+// eps) * gain.  Rows past nt give zero hb rows.  One CTA per token row; the
+// row stays in registers between the two passes (d <= 4 PF_NT PF_RN).
+constexpr int PF_RN = 8;   // float4 groups per thread
 __global__ void k_pf_resid_norm(float* x, const float* part, int splits, int ntp, int d, const __nv_bfloat16* gain,
                                 float eps, int nt, __nv_bfloat16* hb) {
     __shared__ float red[PF_NT / 32];
     const int t = blockIdx.x;
     float* xr = x + (size_t)t * d;
+    float4 v[PF_RN];
     float ss = 0.f;
-    for (int i = threadIdx.x * 4; i < d; i += blockDim.x * 4) {
-        float4 v = *reinterpret_cast<const float4*>(xr + i);
-        if (part && t < nt) {
-            for (int s = 0; s < splits; ++s) {
-                const float4 p = __ldg(reinterpret_cast<const float4*>(part + ((size_t)s * ntp + t) * d + i));
-                v.x += p.x; v.y += p.y; v.z += p.z; v.w += p.w;
-            }
-            *reinterpret_cast<float4*>(xr + i) = v;
+#pragma unroll
+    for (int j = 0; j < PF_RN; ++j) {
+        const int i = (threadIdx.x + j * PF_NT) * 4;
+        if (i < d) {
+            v[j] = *reinterpret_cast<const float4*>(xr + i);
+            if (part && t < nt)
+                for (int s = 0; s < splits; ++s)
+                    v[j] = f4add(v[j], __ldg(reinterpret_cast<const float4*>(part + ((size_t)s * ntp + t) * d + i)));
         }
-        ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+    }
+#pragma unroll
+    for (int j = 0; j < PF_RN; ++j) {
+        const int i = (threadIdx.x + j * PF_NT) * 4;
+        if (i < d) {
+            if (part && t < nt) *reinterpret_cast<float4*>(xr + i) = v[j];
+            ss = fmaf(v[j].x, v[j].x, fmaf(v[j].y, v[j].y, fmaf(v[j].z, v[j].z, fmaf(v[j].w, v[j].w, ss))));
+        }
     }
     if (!gain) return;
     const float tot = block_sum(ss, red);
     const float inv = 1.0f / sqrtf(tot / (float)d + eps);
-    for (int i = threadIdx.x * 4; i < d; i += blockDim.x * 4) {
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (t < nt) {
-            const float4 xv = *reinterpret_cast<const float4*>(xr + i);
-            v = make_float4(xv.x * inv * __bfloat162float(gain[i]), xv.y * inv * __bfloat162float(gain[i + 1]),
-                            xv.z * inv * __bfloat162float(gain[i + 2]), xv.w * inv * __bfloat162float(gain[i + 3]));
+#pragma unroll
+    for (int j = 0; j < PF_RN; ++j) {
+        const int i = (threadIdx.x + j * PF_NT) * 4;
+        if (i < d) {
+            const uint2 gr = __ldg(reinterpret_cast<const uint2*>(gain + i));
+            const float2 g01 = bf16x2_to_f2(gr.x), g23 = bf16x2_to_f2(gr.y);
+            const float4 o = t < nt ? make_float4(v[j].x * inv * g01.x, v[j].y * inv * g01.y, v[j].z * inv * g23.x,
+                                                  v[j].w * inv * g23.y)
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+            put_hilo4(hb, d, t, i, o);
         }
-        put_hilo4(hb, d, t, i, v);
     }
 }
 
@@ -136,9 +157,6 @@ __device__ __forceinline__ size_t kv_off(const PfKv& kv, int g, int pos) {
 // Four consecutive dims per thread and step (16-byte loads), every load of a
 // step issued before its arithmetic; the partial sums, the RoPE table and the
 // page table are read-only here (non-coherent loads).
-__device__ __forceinline__ float4 f4add(float4 a, float4 b) {
-    return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
-}
 __global__ void k_pf_qkv(const float* part, int splits, int ntp, int Hq, int nt, int pos0, const float2* rope,
                          float* qout, PfKv kv) {
     const int t = blockIdx.x;
@@ -476,6 +494,7 @@ bool prefill_supported(const PrefillArgs& a) {
     const int G = a.Hq / a.Hkv;
     if (G != 2 && G != 4) return false;
     if (a.d % PF_BK || qd % PF_BK || a.F % PF_BK) return false;
+    if (a.d > 4 * PF_NT * PF_RN) return false;   // the norm kernel's row in registers
     return true;
 }
 

@@ -299,8 +299,9 @@ int dec_prefill(dec_handle *h, const int32_t *pages, const int32_t *tokens, int3
 /* Multi-token prefill of ONE sequence as a block step ("Models, Registry and
  * the Driver", section "The Model": a step shape is rows x new tokens;
  * positions are absolute, so a prefill is a step continuing from a position).
- * The n tokens at positions pos0 .. pos0 + n - 1 run in blocks of 128 tokens:
- * per layer the projections are dense contractions on the tensor cores
+ * The n tokens at positions pos0 .. pos0 + n - 1 run layer by layer in passes
+ * of up to 1024 tokens (blocks of 128 for the tensor cores): per layer the
+ * projections are dense contractions on the tensor cores
  * (tcgen05.mma, bf16 weights, activations as bf16 hi + lo parts, fp32
  * accumulation), attention is causal over every position up to each token
  * (online softmax, fp32), and every layer's K/V of the n positions is written
@@ -316,8 +317,9 @@ int dec_prefill(dec_handle *h, const int32_t *pages, const int32_t *tokens, int3
  *   id_out      host, the greedy id after the last token, or NULL
  * Positions before pos0 must already hold the sequence's K/V (from steps or an
  * earlier prefill).  Any capture with bf16 weights and K/V whose shape has
- * head_dim 64 or 128, n_heads / n_kv_heads of 2 or 4, and d_model, n_heads *
- * head_dim and ffn_hidden multiples of 64 (DEC_E_UNSUPPORTED otherwise).  The
+ * head_dim 64 or 128, n_heads / n_kv_heads of 2 or 4, d_model, n_heads *
+ * head_dim and ffn_hidden multiples of 64 and d_model <= 8192
+ * (DEC_E_UNSUPPORTED otherwise).  The
  * first call allocates the block's device buffers (cudaMalloc, kept until
  * dec_destroy); the call is synchronous (bounded wait) and must not be
  * captured.  Results agree with stepping the tokens one at a time within the

@@ -107,6 +107,27 @@ def test_prefill_block_8b_shape():
     dec.close()
 
 
+def test_prefill_block_8b_shape_1024_tokens():
+    # a full pass of 8 token blocks at the 8B shape: the O and down projections
+    # run unsplit and add into the residual rows in their own epilogue
+    wl = gen.WORKLOADS["8b"].replace(name="8b_pfb1k", n_layers=1, cap=1024, vocab=4096, positions=())
+    dec, mw = make_decoder(wl)
+    toks = gen.prompt_tokens(wl, n=1024)
+    logits, pick = dec.prefill_block(toks, 0)
+    _check(dec, wl, mw, toks, logits, pick, what="8B-shape 1024-token prefill")
+    dec.close()
+
+
+def test_prefill_block_two_passes():
+    # 1300 tokens: a pass of 1024 and one of 276 that attends to the first pass's K/V
+    wl = gen.WORKLOADS["1b"].replace(name="1b_pfb2p", n_layers=2, cap=1536, vocab=2048)
+    dec, mw = make_decoder(wl)
+    toks = gen.prompt_tokens(wl, n=1300)
+    logits, pick = dec.prefill_block(toks, 0)
+    _check(dec, wl, mw, toks, logits, pick, what="two-pass prefill")
+    dec.close()
+
+
 def test_prefill_block_refusals():
     wl = gen.WORKLOADS["1b"].replace(name="1b_pfbr", n_layers=1, cap=256)
     dec, _ = make_decoder(wl)
