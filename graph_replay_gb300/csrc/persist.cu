@@ -114,7 +114,7 @@ __device__ __forceinline__ bool ps_poll_ge(const unsigned* p, unsigned target, c
     return false;
 }
 
-template <int HD, int G>
+template <int HD, int G, int R>
 struct PsShared {
     uint64_t full_bar[PS_S];   // a ring slot's copy landed (producer's expect_tx + the copy bytes)
     uint64_t empty_bar[PS_S];  // every compute warp is done with the slot
@@ -124,12 +124,12 @@ struct PsShared {
     // and a stage that CTA 0's producer never issues (-1: none)
     uint32_t spin, ring_polls;
     int hold_phase, drop_stage;
-    float nrm[PS_CW];
+    float nrm[PS_CW * R];   // per (compute warp, decode row): sum of squares of the warp's K-slice
     float wm[PS_AW][8], wl[PS_AW][8], wf[PS_AW][8];   // per (attention warp, head): max, sum, merge factor
     float hm[8], hl[8];                               // per head: the split's max and sum
     union {
         struct {
-            float red[PS_RED_ROWS][PS_SL];   // slice partial sums of pending rows
+            float red[PS_RED_ROWS * R][PS_SL];   // slice partial sums of pending (weight row, decode row) pairs
             float res[PS_MAX_RES];           // residual rows (EPI_ADD)
         } gv;
         struct {
@@ -148,10 +148,11 @@ struct GvGeom {
     int N, K, rps;
 };
 
-template <int HD, int G, bool PAGED>
+template <int HD, int G, bool PAGED, int R>
 struct PsState {
+    static constexpr int NR = R;   // decode rows of the step
     const PersistParams& P;
-    PsShared<HD, G>& sh;
+    PsShared<HD, G, R>& sh;
     unsigned char* ring;
     int cta, nc, np, tid;
     int cons;   // stages consumed (uniform over the CTA)
@@ -163,7 +164,7 @@ struct PsState {
     static constexpr int TILE = PPS * HD * 2;            // bytes of the K (or V) tile
     static constexpr int SUB = HD / 64;
 
-    __device__ PsState(const PersistParams& p, PsShared<HD, G>& s, unsigned char* r, bool trace_on)
+    __device__ PsState(const PersistParams& p, PsShared<HD, G, R>& s, unsigned char* r, bool trace_on)
         : P(p), sh(s), ring(r), cta(blockIdx.x), nc(gridDim.x), np(5 * p.L + 2), tid(threadIdx.x), cons(0),
           trace(trace_on ? p.trace : nullptr) {}
 
@@ -446,19 +447,25 @@ __device__ __forceinline__ float rows_reduce(float (&v)[RU], int lane, int& row)
 }
 
 // One GEMV phase over this CTA's rows: warp w owns K-slice w of every row, with
-// the slice's activations in registers; each lane's partial sums are reduced
-// over the warp, the slices' sums wait in shared memory and are added in slice
-// order (fixed order: no atomics) when a chunk of PS_RED_ROWS rows is complete.
-// Stages carry no CTA-wide barrier: a warp releases a stage when it is done.
-template <int CPL, int PRO, int EPI, int HD, int G, bool PAGED>
-__device__ __forceinline__ void ps_gemv(PsState<HD, G, PAGED>& st, const GvGeom& g, const float* act,
+// the slice's activations of each decode row in registers; each lane's partial
+// sums are reduced over the warp, the slices' sums wait in shared memory and
+// are added in slice order (fixed order: no atomics) when a chunk of
+// PS_RED_ROWS weight rows is complete.  Stages carry no CTA-wide barrier: a
+// warp releases a stage when it is done.  Decode row r of the activations and
+// of the output sits at r * K and r * N (r * n[0] for the SwiGLU pair).
+template <int CPL, int PRO, int EPI, int HD, int G, bool PAGED, int R>
+__device__ __forceinline__ void ps_gemv(PsState<HD, G, PAGED, R>& st, const GvGeom& g, const float* act,
                                         const __nv_bfloat16* gain, float* out, int phase) {
-    using ST = PsState<HD, G, PAGED>;
+    using ST = PsState<HD, G, PAGED, R>;
     constexpr int VEC = 8;
-    // rows per pass: a slot holds PS_SLOT / (4096 CPL) rows of K = 2048 CPL (rounded to a power of two)
+    // weight rows per pass: a slot holds PS_SLOT / (4096 CPL) rows of K = 2048 CPL (rounded to a
+    // power of two), divided among the decode rows so that a lane keeps at most 16 sums
     constexpr int RU0 = PS_SLOT / (4096 * CPL) > 0 ? PS_SLOT / (4096 * CPL) : 1;
-    constexpr int RU = RU0 >= 16 ? 16 : (RU0 >= 8 ? 8 : (RU0 >= 4 ? 4 : (RU0 >= 2 ? 2 : 1)));
-    static_assert((RU & (RU - 1)) == 0, "rows per pass must be a power of two");
+    constexpr int RU1 = RU0 >= 16 ? 16 : (RU0 >= 8 ? 8 : (RU0 >= 4 ? 4 : (RU0 >= 2 ? 2 : 1)));
+    constexpr int RU = RU1 / R >= 1 ? RU1 / R : 1;
+    constexpr int RS = RU * R;   // sums per lane and pass
+    constexpr bool TWO = R == 1 || RS < 4;   // two FMA chains per sum, unless several rows give the ILP
+    static_assert((RU & (RU - 1)) == 0 && (R & (R - 1)) == 0 && RS <= 16, "rows per pass must be a power of two");
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int K = g.K;
     const int SWV = K / (PS_SL * VEC);
@@ -473,8 +480,9 @@ __device__ __forceinline__ void ps_gemv(PsState<HD, G, PAGED>& st, const GvGeom&
     }
     const int rps = g.rps;
     const int nst = (row1 - row0 + rps - 1) / rps;
-    const int chunk = (PS_RED_ROWS / rps) * rps;   // rows per flush, whole stages
+    const int chunk = (PS_RED_ROWS / rps) * rps;   // weight rows per flush, whole stages
     const size_t row_bytes = (size_t)K * 2;
+    const int ostride = EPI == EPI_SWIGLU_PAIR ? g.n[0] : g.N;   // output row stride per decode row
     auto& sh = st.sh;
 
     // the norm gains do not depend on the previous phase: load them before its wait
@@ -486,43 +494,57 @@ __device__ __forceinline__ void ps_gemv(PsState<HD, G, PAGED>& st, const GvGeom&
     st.grid_wait(phase - 1);
     if (tid == 0 && st.trace) trace_mark(st.trace, phase, 1);
 
-    // prologue: this lane's activations (its slice columns), in registers; the
-    // slices of the compute warps cover K exactly, so they also give the norm
-    float areg[CPL][VEC];
+    // prologue: this lane's activations (its slice columns) of every decode row,
+    // in registers; the slices of the compute warps cover K exactly, so they
+    // also give the norms
+    float areg[R][CPL][VEC];
 #pragma unroll
-    for (int j = 0; j < CPL; ++j) {
-        const int c = (vbase + lane + 32 * j) * VEC;
-        const float4 x0 = ldcg4(act + c), x1 = ldcg4(act + c + 4);
-        areg[j][0] = x0.x; areg[j][1] = x0.y; areg[j][2] = x0.z; areg[j][3] = x0.w;
-        areg[j][4] = x1.x; areg[j][5] = x1.y; areg[j][6] = x1.z; areg[j][7] = x1.w;
-    }
-    if (PRO == PRO_RMSNORM) {
-        float ss = 0.f;
-#pragma unroll
-        for (int j = 0; j < CPL; ++j)
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) ss = fmaf(areg[j][e], areg[j][e], ss);
-        ss = warp_sum(ss);
-        if (lane == 0) sh.nrm[warp] = ss;
-        ST::csync();
-        float t = 0.f;
-#pragma unroll
-        for (int w = 0; w < PS_CW; ++w) t += sh.nrm[w];
-        const float inv = 1.0f / sqrtf(t / (float)K + st.P.eps);
+    for (int r = 0; r < R; ++r)
 #pragma unroll
         for (int j = 0; j < CPL; ++j) {
-            float gf[VEC];
-            Elem<__nv_bfloat16>::unpack(graw[j], gf);
+            const int c = (vbase + lane + 32 * j) * VEC;
+            const float4 x0 = ldcg4(act + (size_t)r * K + c), x1 = ldcg4(act + (size_t)r * K + c + 4);
+            areg[r][j][0] = x0.x; areg[r][j][1] = x0.y; areg[r][j][2] = x0.z; areg[r][j][3] = x0.w;
+            areg[r][j][4] = x1.x; areg[r][j][5] = x1.y; areg[r][j][6] = x1.z; areg[r][j][7] = x1.w;
+        }
+    if (PRO == PRO_RMSNORM) {
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) areg[j][e] = areg[j][e] * inv * gf[e];
+        for (int r = 0; r < R; ++r) {
+            float ss = 0.f;
+#pragma unroll
+            for (int j = 0; j < CPL; ++j)
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) ss = fmaf(areg[r][j][e], areg[r][j][e], ss);
+            ss = warp_sum(ss);
+            if (lane == 0) sh.nrm[warp * R + r] = ss;
+        }
+        ST::csync();
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            float t = 0.f;
+#pragma unroll
+            for (int w = 0; w < PS_CW; ++w) t += sh.nrm[w * R + r];
+            const float inv = 1.0f / sqrtf(t / (float)K + st.P.eps);
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) {
+                float gf[VEC];
+                Elem<__nv_bfloat16>::unpack(graw[j], gf);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) areg[r][j][e] = areg[r][j][e] * inv * gf[e];
+            }
         }
     }
-    const bool res_local = EPI == EPI_ADD && (row1 - row0) <= PS_MAX_RES;
+    const bool res_local = R == 1 && EPI == EPI_ADD && (row1 - row0) <= PS_MAX_RES;
     if (EPI == EPI_ADD && res_local)   // read before this phase writes any row; used after a barrier
         for (int i = tid; i < row1 - row0; i += PS_CT) sh.sc.gv.res[i] = __ldcg(out + row0 + i);
 
-    unsigned long long best = 0ull;
-    bool nonfin = false;
+    unsigned long long best[R];
+    bool nonfin[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        best[r] = 0ull;
+        nonfin[r] = false;
+    }
     bool live_all = true;
     int c0 = 0;   // first row (within the CTA's rows) of the pending chunk
     for (int k = 0; k < nst; ++k) {
@@ -532,38 +554,57 @@ __device__ __forceinline__ void ps_gemv(PsState<HD, G, PAGED>& st, const GvGeom&
         const bool live = !*reinterpret_cast<volatile int*>(&sh.abort);
         live_all = live_all && live;
         for (int m0 = 0; m0 < nr; m0 += RU) {
-            float acc[RU], acc2[RU];
+            float acc[RS], acc2[RS];   // sum u * R + r: weight row m0 + u, decode row r
 #pragma unroll
-            for (int u = 0; u < RU; ++u) acc[u] = acc2[u] = 0.f;
+            for (int u = 0; u < RS; ++u) acc[u] = acc2[u] = 0.f;
             // slices are exactly 32 * CPL vectors wide (the plan admits no other K);
             // rows of the last pass beyond nr re-read row nr - 1, results dropped
             if (live) {
+                // the pass's weight vectors: all loaded up front while the activations leave
+                // room in the registers, else each just before its use
+                constexpr bool PRE = R * CPL * VEC <= 64;
                 uint4 wv[RU][CPL];
+                if (PRE) {
 #pragma unroll
-                for (int u = 0; u < RU; ++u) {
-                    const int iu = min(m0 + u, nr - 1);
-                    const uint4* wr = reinterpret_cast<const uint4*>(stg + (size_t)iu * row_bytes);
+                    for (int u = 0; u < RU; ++u) {
+                        const int iu = min(m0 + u, nr - 1);
+                        const uint4* wr = reinterpret_cast<const uint4*>(stg + (size_t)iu * row_bytes);
 #pragma unroll
-                    for (int j = 0; j < CPL; ++j) wv[u][j] = wr[vbase + lane + 32 * j];
+                        for (int j = 0; j < CPL; ++j) wv[u][j] = wr[vbase + lane + 32 * j];
+                    }
                 }
 #pragma unroll
                 for (int u = 0; u < RU; ++u)
 #pragma unroll
                     for (int j = 0; j < CPL; ++j) {
                         float wf[VEC];
-                        Elem<__nv_bfloat16>::unpack(wv[u][j], wf);
-#pragma unroll
-                        for (int e = 0; e < VEC; e += 2) {
-                            acc[u] = fmaf(wf[e], areg[j][e], acc[u]);
-                            acc2[u] = fmaf(wf[e + 1], areg[j][e + 1], acc2[u]);
+                        if (PRE) {
+                            Elem<__nv_bfloat16>::unpack(wv[u][j], wf);
+                        } else {
+                            const uint4* wr =
+                                reinterpret_cast<const uint4*>(stg + (size_t)min(m0 + u, nr - 1) * row_bytes);
+                            Elem<__nv_bfloat16>::unpack(wr[vbase + lane + 32 * j], wf);
                         }
+#pragma unroll
+                        for (int r = 0; r < R; ++r)
+#pragma unroll
+                            for (int e = 0; e < VEC; e += 2) {
+                                acc[u * R + r] = fmaf(wf[e], areg[r][j][e], acc[u * R + r]);
+                                if (TWO)
+                                    acc2[u * R + r] = fmaf(wf[e + 1], areg[r][j][e + 1], acc2[u * R + r]);
+                                else
+                                    acc[u * R + r] = fmaf(wf[e + 1], areg[r][j][e + 1], acc[u * R + r]);
+                            }
                     }
             }
+            if (TWO) {
 #pragma unroll
-            for (int u = 0; u < RU; ++u) acc[u] += acc2[u];
+                for (int u = 0; u < RS; ++u) acc[u] += acc2[u];
+            }
             int ru;
-            const float t = rows_reduce<RU>(acc, lane, ru);
-            if ((lane & (32 / RU - 1)) == 0 && m0 + ru < nr) sh.sc.gv.red[a - c0 + m0 + ru][slice] = t;
+            const float t = rows_reduce<RS>(acc, lane, ru);   // ru = u * R + r
+            if ((lane & (32 / RS - 1)) == 0 && m0 + ru / R < nr)
+                sh.sc.gv.red[(a - c0 + m0) * R + ru][slice] = t;
         }
         st.stage_release();
         // a full chunk (or the phase's last rows): add the slices, write the rows
@@ -572,30 +613,37 @@ __device__ __forceinline__ void ps_gemv(PsState<HD, G, PAGED>& st, const GvGeom&
             ST::csync();
             if (EPI == EPI_SWIGLU_PAIR && live_all) {   // one flush holds both halves (the plan checks it)
                 const int n = (row1 - row0) / 2;
-                for (int i = tid; i < n; i += PS_CT) {
+                for (int ir = tid; ir < n * R; ir += PS_CT) {
+                    const int i = ir / R, r = ir % R;
                     float gs = 0.f, us = 0.f;
 #pragma unroll
                     for (int w = 0; w < PS_SL; ++w) {
-                        gs += sh.sc.gv.red[i][w];
-                        us += sh.sc.gv.red[n + i][w];
+                        gs += sh.sc.gv.red[i * R + r][w];
+                        us += sh.sc.gv.red[(n + i) * R + r][w];
                     }
-                    out[row0 + i] = gs / (1.0f + expf(-gs)) * us;
+                    out[(size_t)r * ostride + row0 + i] = gs / (1.0f + expf(-gs)) * us;
                 }
             } else if (live_all) {
-                for (int i = tid; i < done - c0; i += PS_CT) {
+                for (int ir = tid; ir < (done - c0) * R; ir += PS_CT) {
+                    const int i = ir / R, r = ir % R;
                     const int row = row0 + c0 + i;
                     float t = 0.f;
 #pragma unroll
-                    for (int w = 0; w < PS_SL; ++w) t += sh.sc.gv.red[i][w];
+                    for (int w = 0; w < PS_SL; ++w) t += sh.sc.gv.red[i * R + r][w];
+                    float* o = out + (size_t)r * ostride + row;
                     if (EPI == EPI_ADD) {
-                        out[row] = (res_local ? sh.sc.gv.res[row - row0] : __ldcg(out + row)) + t;
+                        *o = (res_local ? sh.sc.gv.res[row - row0] : __ldcg(o)) + t;
                     } else {
-                        out[row] = t;
+                        *o = t;
                     }
                     if (EPI == EPI_LOGITS) {
-                        if (!isfinite(t)) nonfin = true;
-                        const unsigned long long key = argmax_key(t, row);
-                        best = key > best ? key : best;
+#pragma unroll
+                        for (int q = 0; q < R; ++q)
+                            if (q == r) {
+                                if (!isfinite(t)) nonfin[q] = true;
+                                const unsigned long long key = argmax_key(t, row);
+                                best[q] = key > best[q] ? key : best[q];
+                            }
                     }
                 }
             }
@@ -605,22 +653,25 @@ __device__ __forceinline__ void ps_gemv(PsState<HD, G, PAGED>& st, const GvGeom&
     }
     if (EPI == EPI_LOGITS) {
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
-            best = other > best ? other : best;
-        }
-        const bool any_nf = __any_sync(0xffffffffu, nonfin);
-        if (lane == 0) {
-            if (best) atomicMax(st.P.amax, best);
-            if (any_nf) atomicOr(st.P.nonfinite, 1u);
+        for (int r = 0; r < R; ++r) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const unsigned long long other = __shfl_xor_sync(0xffffffffu, best[r], o);
+                best[r] = other > best[r] ? other : best[r];
+            }
+            const bool any_nf = __any_sync(0xffffffffu, nonfin[r]);
+            if (lane == 0) {
+                if (best[r]) atomicMax(st.P.amax + r, best[r]);
+                if (any_nf) atomicOr(st.P.nonfinite + r, 1u);
+            }
         }
     }
 }
 
 // ---------------- attention phase (tensor cores, as attn_mma.cu) ----------------
-template <int HD, int G, bool PAGED>
-__device__ __forceinline__ void ps_attention(PsState<HD, G, PAGED>& st, int l) {
-    using ST = PsState<HD, G, PAGED>;
+template <int HD, int G, bool PAGED, int R>
+__device__ __forceinline__ void ps_attention(PsState<HD, G, PAGED, R>& st, int l) {
+    using ST = PsState<HD, G, PAGED, R>;
     constexpr int PPS = ST::PPS, TILE = ST::TILE;
     constexpr int KPW = PPS / PS_AW, BLK = KPW / 16, KSTEP = HD / 16, DT = HD / 16;
     static_assert(G <= 4, "P^T columns hold G heads' bf16 parts and G remainders");
@@ -942,13 +993,13 @@ __device__ __forceinline__ void ps_attention(PsState<HD, G, PAGED>& st, int l) {
     }
 }
 
-template <int CPL_D, int CPL_F, int HD, int G, bool PAGED>
+template <int CPL_D, int CPL_F, int HD, int G, bool PAGED, int R>
 __global__ void __launch_bounds__(PS_THREADS, 1) k_persist(const __grid_constant__ PersistParams P) {
     extern __shared__ __align__(1024) unsigned char ps_raw[];
     unsigned char* ring =
         reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(ps_raw) + 1023) & ~(uintptr_t)1023);
-    __shared__ PsShared<HD, G> sh;
-    using ST = PsState<HD, G, PAGED>;
+    __shared__ PsShared<HD, G, R> sh;
+    using ST = PsState<HD, G, PAGED, R>;
     const int tid = threadIdx.x;
 
     if (tid == 0) {
@@ -1011,7 +1062,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) k_persist(const __grid_constant
                     }
                 }
             } else if (k == PK_ATTN) {
-                ps_attention<HD, G, PAGED>(st, st.layer(p));
+                ps_attention<HD, G, PAGED, R>(st, st.layer(p));
             } else {
                 GvGeom g;
                 const int l = k == PK_HEAD ? 0 : st.layer(p);
@@ -1062,13 +1113,23 @@ __global__ void __launch_bounds__(PS_THREADS, 1) k_persist(const __grid_constant
 
 template <int CPL_D, int CPL_F, int HD, int G>
 static const void* ps_pick_paged(bool paged) {
-    return paged ? (const void*)&k_persist<CPL_D, CPL_F, HD, G, true>
-                 : (const void*)&k_persist<CPL_D, CPL_F, HD, G, false>;
+    return paged ? (const void*)&k_persist<CPL_D, CPL_F, HD, G, true, 1>
+                 : (const void*)&k_persist<CPL_D, CPL_F, HD, G, false, 1>;
 }
-// instantiated shapes: (d, F, hd, G) of the 8B-shape and 1B-class decoders
-static const void* ps_pick(int cpl_d, int cpl_f, int hd, int G, bool paged) {
-    if (cpl_d == 2 && cpl_f == 7 && hd == 128 && G == 4) return ps_pick_paged<2, 7, 128, 4>(paged);
-    if (cpl_d == 1 && cpl_f == 4 && hd == 64 && G == 4) return ps_pick_paged<1, 4, 64, 4>(paged);
+// instantiated shapes: (d, F, hd, G) of the 8B-shape and 1B-class decoders at
+// one row; the 1B-class decoder with contiguous K/V also at 2 and 4 rows (its
+// down projection's K-slice of 4 rows is 128 activations per thread, the
+// most the register file holds next to the rest)
+static const void* ps_pick(int cpl_d, int cpl_f, int hd, int G, bool paged, int R) {
+    if (R == 1) {
+        if (cpl_d == 2 && cpl_f == 7 && hd == 128 && G == 4) return ps_pick_paged<2, 7, 128, 4>(paged);
+        if (cpl_d == 1 && cpl_f == 4 && hd == 64 && G == 4) return ps_pick_paged<1, 4, 64, 4>(paged);
+        return nullptr;
+    }
+    if (!paged && cpl_d == 1 && cpl_f == 4 && hd == 64 && G == 4) {
+        if (R == 2) return (const void*)&k_persist<1, 4, 64, 4, false, 2>;
+        if (R == 4) return (const void*)&k_persist<1, 4, 64, 4, false, 4>;
+    }
     return nullptr;
 }
 
@@ -1076,13 +1137,12 @@ static int cpl_of(int K) { return (K / (PS_SL * 8) + 31) / 32; }
 
 cudaError_t persist_plan(PersistPlan* plan, int num_sms) {
     PersistParams& p = plan->p;
-    if (p.R != 1) return cudaErrorNotSupported;
     if (p.Hq * p.hd != p.d) return cudaErrorNotSupported;   // O-proj uses the d-column variant
     if (p.d % (PS_SL * 8 * 32) || p.F % (PS_SL * 8 * 32)) return cudaErrorNotSupported;
     const int cd = cpl_of(p.d), cf = cpl_of(p.F);
     if (p.d / (PS_SL * 8) != 32 * cd || p.F / (PS_SL * 8) != 32 * cf) return cudaErrorNotSupported;
     const int G = p.Hq / p.Hkv;
-    const void* fn = ps_pick(cd, cf, p.hd, G, p.paged != 0);
+    const void* fn = ps_pick(cd, cf, p.hd, G, p.paged != 0, p.R);
     if (!fn) return cudaErrorNotSupported;
     // rows per 64 KB stage (whole rows, a multiple of the row groups' loads)
     auto rps_for = [&](int K, int cpl) {

@@ -30,7 +30,7 @@ def _oracle_flag(logits) -> int:
     return int(not np.isfinite(np.asarray(logits)).all())
 
 
-@pytest.mark.parametrize("strategy, rows", [("graph", 2), ("persistent", 1)])
+@pytest.mark.parametrize("strategy, rows", [("graph", 2), ("persistent", 1), ("persistent", 2)])
 def test_nonfinite_flag_follows_the_row(strategy, rows):
     import torch
     wl = ONE_B_2L.replace(rows=rows)
@@ -62,7 +62,7 @@ def test_nonfinite_flag_follows_the_row(strategy, rows):
     dec.close()
 
 
-@pytest.mark.parametrize("strategy, rows", [("graph", 2), ("persistent", 1)])
+@pytest.mark.parametrize("strategy, rows", [("graph", 2), ("persistent", 1), ("persistent", 4)])
 def test_nonfinite_flag_from_the_head(strategy, rows):
     import torch
     wl = ONE_B_2L.replace(rows=rows)

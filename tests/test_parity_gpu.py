@@ -118,10 +118,11 @@ def test_8b_decode_at_prefilled_positions():
 
 
 @pytest.mark.slow
-def test_1b_long_cap_rows4():
+@pytest.mark.parametrize("strategy", ["graph", "persistent"])
+def test_1b_long_cap_rows4(strategy):
     # configuration 5: cap 32768, 4 rows at pos {100, 8000, 20000, 32767}
     wl = gen.WORKLOADS["1b_long"]
-    dec, mw = make_decoder(wl)
+    dec, mw = make_decoder(wl, strategy=strategy)
     positions = gen.row_positions(wl)
     toks = gen.prompt_tokens(wl, n=wl.rows)
     from gen.device import place_kv

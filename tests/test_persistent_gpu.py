@@ -8,7 +8,8 @@ import pytest
 
 import gen
 import oracle
-from _harness import assert_close, make_decoder, paged_case, prefilled_positions_case, run_sequence
+from _harness import (assert_close, assert_greedy, make_decoder, paged_case, prefilled_positions_case,
+                      run_sequence)
 
 pytestmark = pytest.mark.gpu
 
@@ -103,6 +104,62 @@ def test_persistent_kv_write_touches_only_pos():
 
 def test_persistent_paged_1b_row1():
     paged_case("1b", 1, 6, n_layers=4, **PERSIST)
+
+
+def _rows_case(rows, n_steps, n_layers=4, cap=1024, eager_check=True):
+    """Rows at independent positions with K/V pre-filled N(0,1) below each row's
+    start, stepped together through the persistent kernel and compared with one
+    oracle per row; replaying the same steps eagerly gives the same bits."""
+    import torch
+    from gen.device import place_kv
+    wl = gen.WORKLOADS["1b"].replace(name=f"1b_prows{rows}", rows=rows, n_layers=n_layers, cap=cap)
+    dec, mw = make_decoder(wl, **PERSIST)
+    st = dec.stats()
+    assert st["strategy"] == 1 and st["kernels_per_step"] == 1
+    start = [int(x) for x in gen.ints(wl.seed, 97, 0, cap - n_steps, rows)]
+    toks = [gen.prompt_tokens(wl, row=r, n=n_steps) for r in range(rows)]
+    orcs = []
+    for r in range(rows):
+        orc = oracle.Oracle(mw, cap=cap)
+        for l in range(n_layers):
+            for which in (0, 1):
+                kv = gen.kv_prefill(wl, l, which, r, start[r])
+                place_kv(dec.kv(l, which), kv, r)
+                (orc.K if which == 0 else orc.V)[0][l][: start[r]] = kv
+        orcs.append(orc)
+    before = [dec.kv(l, w).clone() for l in range(n_layers) for w in (0, 1)]
+
+    def run():
+        out = []
+        for i in range(n_steps):
+            res = dec.step([int(toks[r][i]) for r in range(rows)], [start[r] + i for r in range(rows)])
+            out.append((res.logits.copy(), res.ids.copy(), res.nonfinite.copy()))
+        return out
+
+    got = run()
+    for i, (logits, ids, nf) in enumerate(got):
+        for r in range(rows):
+            ref = orcs[r].step(0, int(toks[r][i]), start[r] + i)
+            assert_close(logits[r], ref, wl, f"rows {rows} row {r} step {i}")
+            assert_greedy(ids[r], ref, f"rows {rows} row {r} step {i}")
+            assert nf[r] == 0
+    if eager_check:
+        kv_graph = [dec.kv(l, w).clone() for l in range(n_layers) for w in (0, 1)]
+        for t, b in zip([dec.kv(l, w) for l in range(n_layers) for w in (0, 1)], before):
+            t.copy_(b)
+        dec.set_eager(True)
+        again = run()
+        dec.set_eager(False)
+        for (a, ia, _), (b, ib, _) in zip(got, again):
+            assert np.array_equal(a, b) and np.array_equal(ia, ib)
+        for a, l_w in zip(kv_graph, [(l, w) for l in range(n_layers) for w in (0, 1)]):
+            assert torch.equal(a, dec.kv(*l_w))
+    dec.close()
+
+
+@pytest.mark.parametrize("rows", [2, 4])
+def test_persistent_1b_rows_at_independent_positions(rows):
+    _rows_case(rows, n_steps=6)
 
 
 def test_persistent_unsupported_shape_is_refused():
