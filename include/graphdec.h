@@ -92,8 +92,10 @@ typedef enum dec_kv_layout { DEC_KV_CONTIGUOUS = 0, DEC_KV_PAGED = 1 } dec_kv_la
  *               summation order: results agree with GRAPH within the parity
  *               tolerances, not bit for bit; replay and eager runs of one
  *               strategy are bit-identical.  Available for bf16 weights and
- *               KV, rows = 1 and the 8B-shape / 1B-class layer shapes
- *               (DEC_E_UNSUPPORTED at capture otherwise). */
+ *               KV with the 8B-shape or 1B-class layer shapes at rows = 1
+ *               (contiguous or paged K/V), and with the 1B-class shape at
+ *               rows = 2 or 4 with contiguous K/V (DEC_E_UNSUPPORTED at
+ *               capture otherwise). */
 typedef enum dec_strategy { DEC_STRATEGY_GRAPH = 0, DEC_STRATEGY_PERSISTENT = 1 } dec_strategy;
 
 /* Which K/V positions the attention of the captured step reads:
