@@ -225,7 +225,9 @@ __device__ __forceinline__ void cp_async_wait_prev() { asm volatile("cp.async.wa
 // the G query heads of kv head g, row r = token * G + head -- and sweeps the
 // keys [0, last position of its tokens] in tiles of PF_KT2 keys, double
 // buffered: the next tile's asynchronous copies are in flight while the
-// current one is computed.  The CTAs with the most keys start first.  Warp w owns
+// current one is computed.  The CTAs with the most keys start first.  Q lives
+// in shared memory (read by ldmatrix at every k-step), so a thread stays under
+// 128 registers and two CTAs share an SM.  Warp w owns
 // query rows 8w..8w+7: the MMA's 16 A rows hold their bf16 parts (rows 0-7) and
 // remainders (rows 8-15), so q keeps about 16 significant bits; S = Q K^T comes
 // out as hi + lo row pairs, and P (online softmax, fp32) goes back into the
@@ -234,19 +236,21 @@ __device__ __forceinline__ void cp_async_wait_prev() { asm volatile("cp.async.wa
 // ldmatrix); V is read transposed.  The output goes to hb as the O projection's
 // hi/lo activation rows.
 constexpr int PF_QR = 64;          // query rows per CTA
-constexpr int PF_KT2 = 64;         // keys per tile
-// dynamic shared memory of the attention kernel: two K and two V tiles
-__host__ __device__ constexpr int pf_attn_smem(int hd) { return 4 * PF_KT2 * (hd + 8) * 2; }
+constexpr int PF_KT2 = 32;         // keys per tile
+// dynamic shared memory of the attention kernel: two K and two V tiles, and the
+// CTA's Q as 8 warps x 16 rows (bf16 parts, then remainders)
+__host__ __device__ constexpr int pf_attn_smem(int hd) { return (4 * PF_KT2 + 128) * (hd + 8) * 2; }
+// 2 CTAs per SM: Q in shared memory and 32-key tiles keep a thread under 128 registers
 template <int HD, int G>
-__global__ void __launch_bounds__(256) k_pf_attn_mma(const float* q, int Hq, int nt, int pos0, float scale, PfKv kv,
-                                                     __nv_bfloat16* hb) {
+__global__ void __launch_bounds__(256, 2) k_pf_attn_mma(const float* q, int Hq, int nt, int pos0, float scale, PfKv kv,
+                                                        __nv_bfloat16* hb) {
     constexpr int KS = HD / 16;            // k-steps of S = Q K^T
     constexpr int DT = HD / 8;             // n-tiles of O
     constexpr int NT = PF_KT2 / 8;         // n-tiles of S
     constexpr int RS = HD + 8;             // shared row stride (bf16)
     constexpr int TPC = PF_QR / G;         // tokens per CTA
     constexpr int TILE = PF_KT2 * RS;      // elements of one K (or V) tile
-    extern __shared__ __align__(16) __nv_bfloat16 pf_kv_smem[];   // K0, K1, V0, V1
+    extern __shared__ __align__(16) __nv_bfloat16 pf_kv_smem[];   // K0, K1, V0, V1, Q
     const int g = blockIdx.y, t0 = (gridDim.x - 1 - blockIdx.x) * TPC, tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tq = lane & 3;
     const int qd = Hq * HD;
@@ -254,24 +258,17 @@ __global__ void __launch_bounds__(256) k_pf_attn_mma(const float* q, int Hq, int
     const int r = warp * 8 + gq, tok = t0 + r / G, head = g * G + r % G;
     const bool live = tok < nt;
     const int qpos = pos0 + tok;
-    // Q fragments: rows 0-7 bf16(q * scale), rows 8-15 the remainders
-    uint32_t qa[KS][4];
-    {
-        const float* qr = q + (size_t)tok * qd + head * HD;
-#pragma unroll
-        for (int k = 0; k < KS; ++k) {
-            float v[4];
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) v[2 * h + e] = live ? qr[16 * k + 8 * h + 2 * tq + e] * scale : 0.f;
-            const float h0 = bf16_round_f(v[0]), h1 = bf16_round_f(v[1]), h2 = bf16_round_f(v[2]), h3 = bf16_round_f(v[3]);
-            qa[k][0] = pack_bf16x2(h0, h1);
-            qa[k][1] = pack_bf16x2(v[0] - h0, v[1] - h1);
-            qa[k][2] = pack_bf16x2(h2, h3);
-            qa[k][3] = pack_bf16x2(v[2] - h2, v[3] - h3);
-        }
+    // this warp's Q as the MMA's A tile: rows 0-7 bf16(q * scale) of its 8 query
+    // rows, rows 8-15 the remainders (read back by ldmatrix at every tile)
+    __nv_bfloat16* q_s = pf_kv_smem + 4 * TILE + warp * 16 * RS;
+    for (int i = lane; i < 8 * HD; i += 32) {
+        const int qr = i / HD, c = i % HD, rw = warp * 8 + qr, tk = t0 + rw / G;
+        const float v = tk < nt ? q[(size_t)tk * qd + (g * G + rw % G) * HD + c] * scale : 0.f;
+        const float hi = bf16_round_f(v);
+        q_s[qr * RS + c] = __float2bfloat16_rn(hi);
+        q_s[(8 + qr) * RS + c] = __float2bfloat16_rn(v - hi);
     }
+    __syncwarp();
     float o[DT][4];
 #pragma unroll
     for (int n = 0; n < DT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
@@ -313,14 +310,17 @@ __global__ void __launch_bounds__(256) k_pf_attn_mma(const float* q, int Hq, int
         for (int n = 0; n < NT; ++n) sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.f;
         const int mi = lane >> 3, rr = lane & 7;
 #pragma unroll
-        for (int k = 0; k < KS; ++k)
+        for (int k = 0; k < KS; ++k) {
+            uint32_t qa[4];   // A: (rows 0-7 | 8-15) x (k 0-7 | 8-15) of this k-step
+            ldsm_x4(smem_u32(q_s + (rr + ((mi & 1) << 3)) * RS + 16 * k + ((mi >> 1) << 3)), qa[0], qa[1], qa[2], qa[3]);
 #pragma unroll
             for (int n2 = 0; n2 < NT / 2; ++n2) {   // two n-tiles (16 keys) per ldmatrix
                 uint32_t b0, b1, b2, b3;
                 ldsm_x4(smem_u32(ks + (16 * n2 + rr + ((mi >> 1) << 3)) * RS + 16 * k + ((mi & 1) << 3)), b0, b1, b2, b3);
-                mma_bf16(sacc[2 * n2], qa[k], b0, b1);
-                mma_bf16(sacc[2 * n2 + 1], qa[k], b2, b3);
+                mma_bf16(sacc[2 * n2], qa, b0, b1);
+                mma_bf16(sacc[2 * n2 + 1], qa, b2, b3);
             }
+        }
         // scores of row gq (hi + lo rows), keys 8n + 2tq + e; online softmax over the tile
         float sc[NT][2];
         float mx = -INFINITY;
