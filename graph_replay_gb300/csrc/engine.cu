@@ -226,7 +226,12 @@ int bounded_wait(dec_handle* h) {
                 return fail(h, DEC_E_TIMEOUT, "device wait exceeded %lld ms; handle poisoned",
                             (long long)h->cfg.wait_timeout_ms);
             }
-            if (ms > 2.0) std::this_thread::sleep_for(std::chrono::microseconds(20));
+            // a step takes milliseconds: poll (yielding the core) for the first 50 ms,
+            // since a sleep wakes tens of microseconds late; sleep after that
+            if (ms > 50.0)
+                std::this_thread::sleep_for(std::chrono::microseconds(20));
+            else
+                std::this_thread::yield();
         }
     }
 }

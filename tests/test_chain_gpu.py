@@ -73,6 +73,12 @@ def test_chain_equals_host_fed_steps_rows4():
     _chain_vs_host(wl, 5, 24, [0, 17, 100, 3])
 
 
+def test_chain_equals_host_fed_steps_persistent_rows4():
+    wl = gen.WORKLOADS["1b"].replace(name="1b_c4p", n_layers=2, cap=256, rows=4)
+    _, st = _chain_vs_host(wl, 5, 24, [0, 17, 100, 3], strategy="persistent")
+    assert st["strategy"] == 1
+
+
 def test_chain_equals_host_fed_steps_paged_rows3():
     wl = gen.WORKLOADS["1b"].replace(name="1b_cp3", n_layers=2, cap=256, rows=3, layout="paged",
                                      page_size=16, num_pages=3 * 16 + 5)

@@ -170,6 +170,20 @@ def test_persistent_unsupported_shape_is_refused():
     assert ei.value.status == DEC_E_UNSUPPORTED
 
 
+@pytest.mark.parametrize("base, rows, layout", [("1b", 2, "paged"), ("1b", 3, "contiguous"), ("8b", 2, "contiguous")])
+def test_persistent_multi_row_shapes_without_a_kernel_are_refused(base, rows, layout):
+    # several rows run on the whole-step kernel for the 1B-class shape with
+    # contiguous K/V at 2 or 4 rows only; anything else is refused at capture
+    from graph_replay_gb300._binding import DEC_E_UNSUPPORTED, DecError
+    shape = dict(name=f"{base}_pref{rows}{layout[0]}", rows=rows, n_layers=1, cap=256, vocab=1024, layout=layout)
+    if layout == "paged":
+        shape.update(page_size=16, num_pages=rows * 16 + 3)
+    wl = gen.WORKLOADS[base].replace(**shape)
+    with pytest.raises(DecError) as ei:
+        make_decoder(wl, **PERSIST)
+    assert ei.value.status == DEC_E_UNSUPPORTED
+
+
 @pytest.mark.slow
 def test_persistent_8b_decode_at_prefilled_positions():
     prefilled_positions_case(gen.WORKLOADS["8b"], **PERSIST)
