@@ -128,6 +128,18 @@ def test_prefill_block_two_passes():
     dec.close()
 
 
+@pytest.mark.parametrize("base, n_layers, n", [("1b", 2, 200), ("8b", 1, 150)])
+def test_prefill_block_gqa_group_of_two(base, n_layers, n):
+    # two query heads per kv head: the attention kernel's 32-token query blocks
+    wl = gen.WORKLOADS[base].replace(name=f"{base}_pfbg2", n_kv_heads=gen.WORKLOADS[base].n_heads // 2,
+                                     n_layers=n_layers, cap=512, vocab=2048, positions=())
+    dec, mw = make_decoder(wl)
+    toks = gen.prompt_tokens(wl, n=n)
+    logits, pick = dec.prefill_block(toks, 0)
+    _check(dec, wl, mw, toks, logits, pick, what=f"{base} group-2 prefill")
+    dec.close()
+
+
 def test_prefill_block_refusals():
     wl = gen.WORKLOADS["1b"].replace(name="1b_pfbr", n_layers=1, cap=256)
     dec, _ = make_decoder(wl)
