@@ -1032,11 +1032,14 @@ int dec_prefill_block(dec_handle* h, int32_t row, const int32_t* pages, const in
     a.paged = h->layout == DEC_KV_PAGED;
     a.page = h->page;
     a.ppr = h->ppr;
+    a.rows = h->rows;
+    a.num_pages = h->npages;
     a.rope = h->d_rope;
     a.err = &h->d_status->err;
     if (!prefill_supported(a))
         return fail(h, DEC_E_UNSUPPORTED, "no block prefill for this shape (head_dim 64 or 128, n_heads / n_kv_heads "
-                    "2 or 4, d_model, n_heads * head_dim and ffn_hidden multiples of 64)");
+                    "2 or 4, d_model, n_heads * head_dim and ffn_hidden multiples of 64, d_model <= 8192, pages of "
+                    "at least 8 tokens)");
     if (!tokens || (a.paged && !pages)) return fail(h, DEC_E_INVALID, "tokens (and for paged K/V the pages) are required");
     if (!a.paged && (row < 0 || row >= h->rows)) return fail(h, DEC_E_RANGE, "row %d outside [0, %d)", row, h->rows);
     if (n < 1 || pos0 < 0 || (int64_t)pos0 + n > h->cap)

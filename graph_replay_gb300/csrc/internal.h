@@ -254,6 +254,7 @@ struct PrefillArgs {
     void* const* V;             // host array [L]: V store
     bool paged;
     int page, ppr;              // paged: tokens per page, pages per sequence
+    int rows, num_pages;        // contiguous: the capture's rows; paged: the pool's pages
     const float2* rope;         // device [cap, hd / 2]
     unsigned* err;              // device error word
 };

@@ -210,182 +210,386 @@ __global__ void k_pf_qkv(const float* part, int splits, int ntp, int Hq, int nt,
     }
 }
 
-// 16-byte asynchronous copy global -> shared; zero bytes read (the 16 bytes
-// zero-filled) when !valid
-__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(valid ? 16 : 0)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-// every copy group of this thread but the newest has landed
-__device__ __forceinline__ void cp_async_wait_prev() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+// ---- causal attention on the 5th-generation tensor cores ----
+// A CTA takes 128 query rows (the TMEM lanes): 128 / G tokens x the G query
+// heads of kv head g, row r = token * G + head.  Per 64-key tile:
+//   S = Q K^T        tcgen05.mma, A = Q (bf16 hi rows, then lo rows: two MMAs
+//                    into one accumulator), B = the K tile, D in TMEM (two S
+//                    buffers, so the next tile's S is computed while this one
+//                    is in softmax).  Q carries 1 / sqrt(hd) * log2(e), so
+//                    the softmax works in powers of two
+//   softmax          two threads per row (warps w and w + 4 share TMEM lanes),
+//                    32 keys each: the row's tile max through shared memory,
+//                    p = 2^(s - m) against the row's reference max m, the sum;
+//                    P as bf16 hi + lo rows in shared memory.  The accumulated
+//                    O and l are rescaled (O in TMEM, each thread its half of
+//                    the columns) only when the row max grows by more than
+//                    PA_RESCALE, since O / l is the same for any reference
+//   O += P V         tcgen05.mma, A = P (hi, then lo), B = the V tile read
+//                    MN-major (V is stored key-major), D = O in TMEM
+// K/V tiles arrive by TMA (128-byte swizzle: the layout the MMAs read; one box
+// per 64 keys x 64 dims, or per page x 64 dims) in a ring of stages; the
+// loader warp then zeroes the V rows past the CTA's last position (they may
+// hold any bits, and P = 0 does not clear a NaN).  Warp 8 issues the MMAs.
+// All waits are bounded; one that gives up sets FAULT_WAIT and every role
+// skips the rest.
+constexpr int PA_ROWS = 128;
+constexpr int PA_KT = 64;
+constexpr int PA_SMX = 256;                // softmax threads: warps 0-7
+constexpr int PA_THREADS = PA_SMX + 64;    // + warp 8 (MMA) + warp 9 (K/V loads)
+constexpr int PA_LOAD_T = 32;
+constexpr float PA_RESCALE = 8.0f;         // log2 units: p <= 2^8 between rescales
+constexpr float PA_LOG2E = 1.4426950408889634f;
 
-// Causal attention on the tensor cores (mma.sync m16n8k16, bf16 in, fp32
-// accumulate), flash-style.  A CTA takes 64 query rows -- PF_QR / G tokens x
-// the G query heads of kv head g, row r = token * G + head -- and sweeps the
-// keys [0, last position of its tokens] in tiles of PF_KT2 keys, double
-// buffered: the next tile's asynchronous copies are in flight while the
-// current one is computed.  The CTAs with the most keys start first.  Q lives
-// in shared memory (read by ldmatrix at every k-step), so a thread stays under
-// 128 registers and two CTAs share an SM.  Warp w owns
-// query rows 8w..8w+7: the MMA's 16 A rows hold their bf16 parts (rows 0-7) and
-// remainders (rows 8-15), so q keeps about 16 significant bits; S = Q K^T comes
-// out as hi + lo row pairs, and P (online softmax, fp32) goes back into the
-// next MMA's A fragments the same way, straight from the registers.  K and V
-// tiles are staged in shared memory (rows padded by 16 bytes: conflict-free
-// ldmatrix); V is read transposed.  The output goes to hb as the O projection's
-// hi/lo activation rows.
-constexpr int PF_QR = 64;          // query rows per CTA
-constexpr int PF_KT2 = 32;         // keys per tile
-// dynamic shared memory of the attention kernel: two K and two V tiles, and the
-// CTA's Q as 8 warps x 16 rows (bf16 parts, then remainders)
-__host__ __device__ constexpr int pf_attn_smem(int hd) { return (4 * PF_KT2 + 128) * (hd + 8) * 2; }
-// 2 CTAs per SM: Q in shared memory and 32-key tiles keep a thread under 128 registers
+// K/V ring stages: as many as fit next to Q and P (3 at head_dim 128, 4 at 64)
+__host__ __device__ constexpr int pa_kv_stages(int hd) { return hd >= 128 ? 3 : 4; }
+template <int HD>
+struct PaLayout {
+    static constexpr int NS = pa_kv_stages(HD);
+    static constexpr int QB = PA_ROWS * HD * 2;   // Q hi (or lo): HD / 64 atoms of [128 rows x 128 B]
+    static constexpr int TB = PA_KT * HD * 2;     // a K (or V) tile: HD / 64 atoms of [64 keys x 128 B]
+    static constexpr int PB = PA_ROWS * PA_KT * 2;   // P hi (or lo): one atom of [128 rows x 128 B]
+    static constexpr int Q_HI = 0, Q_LO = QB, KV = 2 * QB;   // stage b: K at KV + 2 b TB, V at KV + (2 b + 1) TB
+    static constexpr int P_HI = KV + 2 * NS * TB, P_LO = P_HI + PB;
+    static constexpr int BYTES = P_LO + PB;
+};
+__host__ __device__ constexpr int pf_attn_tc_smem(int hd) {
+    return 2 * PA_ROWS * hd * 2 + 2 * pa_kv_stages(hd) * PA_KT * hd * 2 + 2 * PA_ROWS * PA_KT * 2 + 1024;
+}
+// byte offset of 16-byte chunk c (8 bf16) of row r in a [rows x 64] bf16 atom, 128-byte swizzle
+__device__ __forceinline__ uint32_t pa_sw(int r, int c) {
+    return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+}
+__device__ __forceinline__ uint64_t pa_desc(uint32_t saddr, uint32_t lbo) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(lbo >> 4) << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// 2^x by the hardware's base-2 exponential (ex2.approx.ftz; relative error about 2^-22)
+__device__ __forceinline__ float pa_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ void tmem_st_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
+        "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
+        "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+// the two softmax warps of a TMEM lane quarter (w and w + 4) meet at barrier 1 + w
+__device__ __forceinline__ void pa_pair_sync(int quarter) {
+    asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
+}
+
+// kvm: this layer's K and V tensor maps (contiguous: rows (row Hkv + g) cap + pos,
+// box 64 x 64; paged: rows (page Hkv + g) page + o, box 64 x page)
 template <int HD, int G>
-__global__ void __launch_bounds__(256, 2) k_pf_attn_mma(const float* q, int Hq, int nt, int pos0, float scale, PfKv kv,
-                                                        __nv_bfloat16* hb) {
-    constexpr int KS = HD / 16;            // k-steps of S = Q K^T
-    constexpr int DT = HD / 8;             // n-tiles of O
-    constexpr int NT = PF_KT2 / 8;         // n-tiles of S
-    constexpr int RS = HD + 8;             // shared row stride (bf16)
-    constexpr int TPC = PF_QR / G;         // tokens per CTA
-    constexpr int TILE = PF_KT2 * RS;      // elements of one K (or V) tile
-    extern __shared__ __align__(16) __nv_bfloat16 pf_kv_smem[];   // K0, K1, V0, V1, Q
-    const int g = blockIdx.y, t0 = (gridDim.x - 1 - blockIdx.x) * TPC, tid = threadIdx.x;
-    const int warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tq = lane & 3;
+__global__ void __launch_bounds__(PA_THREADS, 1) k_pf_attn_tc(const float* q, int Hq, int nt, int pos0, float scale,
+                                                              PfKv kv, const CUtensorMap* kvm, unsigned* err,
+                                                              __nv_bfloat16* hb) {
+    using LY = PaLayout<HD>;
+    constexpr int TPC = PA_ROWS / G;   // tokens per CTA
+    constexpr int NA = HD / 64;        // 64-column atoms along head_dim
+    constexpr int NS = LY::NS;         // K/V ring stages
+    extern __shared__ __align__(1024) unsigned char pa_raw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(pa_raw) + 1023) & ~(uintptr_t)1023);
+    __shared__ __align__(8) uint64_t kv_tma[LY::NS], kv_full[LY::NS], kv_empty[LY::NS], s_full[2], s_free[2], p_full,
+        p_free, mma_done;
+    __shared__ float pmax[2][2][PA_ROWS];   // [tile parity][half][row]: the halves' tile maxima
+    __shared__ float psum[2][PA_ROWS];      // [half][row]: the halves' sums at the end
+    __shared__ uint32_t tmem;
+    __shared__ int aborted;
+    // grid (kv heads, token blocks): CTAs start in x-fastest order, so the token
+    // blocks with the most keys (the last ones) come first for every head
+    const int g = blockIdx.x, t0 = (gridDim.y - 1 - blockIdx.y) * TPC, tid = threadIdx.x, warp = tid >> 5,
+              lane = tid & 31;
     const int qd = Hq * HD;
-    // this lane's query row (warp row gq) and its position
-    const int r = warp * 8 + gq, tok = t0 + r / G, head = g * G + r % G;
-    const bool live = tok < nt;
-    const int qpos = pos0 + tok;
-    // this warp's Q as the MMA's A tile: rows 0-7 bf16(q * scale) of its 8 query
-    // rows, rows 8-15 the remainders (read back by ldmatrix at every tile)
-    __nv_bfloat16* q_s = pf_kv_smem + 4 * TILE + warp * 16 * RS;
-    for (int i = lane; i < 8 * HD; i += 32) {
-        const int qr = i / HD, c = i % HD, rw = warp * 8 + qr, tk = t0 + rw / G;
-        const float v = tk < nt ? q[(size_t)tk * qd + (g * G + rw % G) * HD + c] * scale : 0.f;
-        const float hi = bf16_round_f(v);
-        q_s[qr * RS + c] = __float2bfloat16_rn(hi);
-        q_s[(8 + qr) * RS + c] = __float2bfloat16_rn(v - hi);
-    }
-    __syncwarp();
-    float o[DT][4];
+    const int last = pos0 + min(t0 + TPC, nt) - 1;   // the last key any row of the CTA sees
+    const int ntiles = last / PA_KT + 1;
+    const float qscale = scale * PA_LOG2E;
+
+    // Q of the CTA's rows as bf16 hi and lo A tiles (scaled by log2(e) / sqrt(hd));
+    // every thread's loads are issued before any is used
+    {
+        constexpr int NQ = (PA_ROWS * (HD / 8) + PA_THREADS - 1) / PA_THREADS;   // 8-column chunks per thread
+        float4 qa[NQ][2];
 #pragma unroll
-    for (int n = 0; n < DT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-    float m_run = -INFINITY, l_run = 0.f;
-    const int last = pos0 + min(t0 + TPC, nt) - 1;               // the last key any row of the CTA sees
-    const int wlast = pos0 + min(t0 + (warp * 8 + 7) / G + 1, nt) - 1;   // ... any row of this warp
-    // copies of the tile at key j0 into buffer b (keys past `last` zero-filled)
-    auto load_tile = [&](int j0, int b) {
-        __nv_bfloat16* kd = pf_kv_smem + b * TILE;
-        __nv_bfloat16* vd = pf_kv_smem + (2 + b) * TILE;
-        for (int i = tid; i < PF_KT2 * (HD / 8); i += 256) {   // 16-byte vectors of K and V
-            const int kk = i / (HD / 8), c = i % (HD / 8), j = j0 + kk;
-            const bool in = j <= last;
-            const size_t off = in ? kv_off(kv, g, j) + (size_t)c * 8 : 0;
-            cp_async16(kd + kk * RS + c * 8, kv.K + off, in);
-            cp_async16(vd + kk * RS + c * 8, kv.V + off, in);
+        for (int u = 0; u < NQ; ++u) {
+            const int i = tid + u * PA_THREADS, r = i / (HD / 8), c = i % (HD / 8), tk = t0 + r / G;
+            if (i < PA_ROWS * (HD / 8) && tk < nt) {
+                const float4* src = reinterpret_cast<const float4*>(q + (size_t)tk * qd + (g * G + r % G) * HD + c * 8);
+                qa[u][0] = __ldg(src);
+                qa[u][1] = __ldg(src + 1);
+            } else {
+                qa[u][0] = qa[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
         }
-        cp_async_commit();
+#pragma unroll
+        for (int u = 0; u < NQ; ++u) {
+            const int i = tid + u * PA_THREADS, r = i / (HD / 8), c = i % (HD / 8);
+            if (i >= PA_ROWS * (HD / 8)) continue;
+            const float v[8] = {qa[u][0].x, qa[u][0].y, qa[u][0].z, qa[u][0].w,
+                                qa[u][1].x, qa[u][1].y, qa[u][1].z, qa[u][1].w};
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float x0 = v[2 * e] * qscale, x1 = v[2 * e + 1] * qscale;
+                const float h0 = bf16_round_f(x0), h1 = bf16_round_f(x1);
+                hi[e] = pack_bf16x2(h0, h1);
+                lo[e] = pack_bf16x2(x0 - h0, x1 - h1);
+            }
+            const uint32_t off = (uint32_t)(c / 8) * (PA_ROWS * 128) + pa_sw(r, c % 8);
+            *reinterpret_cast<uint4*>(sm + LY::Q_HI + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(sm + LY::Q_LO + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 256;" ::"r"(smem_u32(&tmem))
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (tid == 0) {
+        for (int b = 0; b < NS; ++b) {
+            mbar_init(&kv_tma[b], 1);
+            mbar_init(&kv_full[b], PA_LOAD_T);
+            mbar_init(&kv_empty[b], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&s_full[b], 1);
+            mbar_init(&s_free[b], PA_SMX);
+        }
+        mbar_init(&p_full, PA_SMX);
+        mbar_init(&p_free, 1);
+        mbar_init(&mma_done, 1);
+        aborted = 0;
+        mbar_fence_init();
+    }
+    fence_proxy_async_smem();   // Q's generic writes before the tensor core reads them
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t dt = tmem;           // S buffers at columns 0 and 64, O at 128
+    volatile int* ab = &aborted;
+    auto give_up = [&]() {
+        *ab = 1;
+        atomicOr(err, FAULT_WAIT);
     };
-    load_tile(0, 0);
-    int it = 0;
-    for (int j0 = 0; j0 <= last; j0 += PF_KT2, ++it) {
-        if (j0 + PF_KT2 <= last) {
-            load_tile(j0 + PF_KT2, (it + 1) & 1);
-        } else {
-            cp_async_commit();   // an empty group: the wait below still means "this tile has landed"
-        }
-        cp_async_wait_prev();
-        __syncthreads();   // every thread's copies of this tile are visible
-        const __nv_bfloat16* ks = pf_kv_smem + (it & 1) * TILE;
-        const __nv_bfloat16* vs = pf_kv_smem + (2 + (it & 1)) * TILE;
-        if (j0 > wlast) {   // every row of this warp is past these keys (masked)
-            __syncthreads();
-            continue;
-        }
-        // S = Q K^T: 16 rows x PF_KT2 keys
-        float sacc[NT][4];
+
+    if (warp == 9) {
+        // ---- K/V loader warp: lane 0 issues the TMA boxes, the warp zeroes late V rows ----
+        for (int j = 0; j < ntiles; ++j) {
+            const int b = j % NS, j0 = j * PA_KT;
+            unsigned char* kd = sm + LY::KV + 2 * b * LY::TB;
+            unsigned char* vd = kd + LY::TB;
+            if (lane == 0) {
+                if (j >= NS && !(*ab) && !mbar_wait(&kv_empty[b], (uint32_t)((j / NS) - 1) & 1u)) give_up();
+                if (!*ab) {
+                    if (kv.pages) {
+                        const int np = (min(j0 + PA_KT - 1, last) - j0) / kv.page + 1;   // pages holding keys <= last
+                        mbar_arrive_expect_tx(&kv_tma[b], (uint32_t)(np * 2 * NA * kv.page * 128));
+                        for (int pi = 0; pi < np; ++pi) {
+                            const int key = j0 + pi * kv.page;
+                            const int y = (kv.pages[key / kv.page] * kv.Hkv + g) * kv.page;
 #pragma unroll
-        for (int n = 0; n < NT; ++n) sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.f;
-        const int mi = lane >> 3, rr = lane & 7;
+                            for (int a = 0; a < NA; ++a) {
+                                const uint32_t o = (uint32_t)a * (PA_KT * 128) + (uint32_t)(pi * kv.page * 128);
+                                tma_load_2d(kd + o, kvm, a * 64, y, &kv_tma[b]);
+                                tma_load_2d(vd + o, kvm + 1, a * 64, y, &kv_tma[b]);
+                            }
+                        }
+                    } else {
+                        const int y = (kv.row * kv.Hkv + g) * kv.cap + j0;
+                        mbar_arrive_expect_tx(&kv_tma[b], (uint32_t)(2 * NA * PA_KT * 128));
 #pragma unroll
-        for (int k = 0; k < KS; ++k) {
-            uint32_t qa[4];   // A: (rows 0-7 | 8-15) x (k 0-7 | 8-15) of this k-step
-            ldsm_x4(smem_u32(q_s + (rr + ((mi & 1) << 3)) * RS + 16 * k + ((mi >> 1) << 3)), qa[0], qa[1], qa[2], qa[3]);
-#pragma unroll
-            for (int n2 = 0; n2 < NT / 2; ++n2) {   // two n-tiles (16 keys) per ldmatrix
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(smem_u32(ks + (16 * n2 + rr + ((mi >> 1) << 3)) * RS + 16 * k + ((mi & 1) << 3)), b0, b1, b2, b3);
-                mma_bf16(sacc[2 * n2], qa, b0, b1);
-                mma_bf16(sacc[2 * n2 + 1], qa, b2, b3);
-            }
-        }
-        // scores of row gq (hi + lo rows), keys 8n + 2tq + e; online softmax over the tile
-        float sc[NT][2];
-        float mx = -INFINITY;
-#pragma unroll
-        for (int n = 0; n < NT; ++n)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int j = j0 + 8 * n + 2 * tq + e;
-                const float v = sacc[n][e] + sacc[n][2 + e];
-                sc[n][e] = (live && j <= qpos) ? v : -INFINITY;
-                mx = fmaxf(mx, sc[n][e]);
-            }
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float mn = fmaxf(m_run, mx);
-        const float alpha = m_run == -INFINITY ? 0.f : expf(m_run - mn);
-        float ps = 0.f;
-        // P as A fragments: per 16 keys (n-tiles 2kk, 2kk+1), rows 0-7 bf16(p), rows 8-15 remainders
-        uint32_t pa[NT / 2][4];
-#pragma unroll
-        for (int kk = 0; kk < NT / 2; ++kk) {
-            float p[4];
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const float s_ = sc[2 * kk + h][e];
-                    const float pv = s_ == -INFINITY ? 0.f : expf(s_ - mn);
-                    p[2 * h + e] = pv;
-                    ps += pv;
+                        for (int a = 0; a < NA; ++a) {
+                            tma_load_2d(kd + a * (PA_KT * 128), kvm, a * 64, y, &kv_tma[b]);
+                            tma_load_2d(vd + a * (PA_KT * 128), kvm + 1, a * 64, y, &kv_tma[b]);
+                        }
+                    }
                 }
-            const float h0 = bf16_round_f(p[0]), h1 = bf16_round_f(p[1]), h2 = bf16_round_f(p[2]), h3 = bf16_round_f(p[3]);
-            pa[kk][0] = pack_bf16x2(h0, h1);
-            pa[kk][1] = pack_bf16x2(p[0] - h0, p[1] - h1);
-            pa[kk][2] = pack_bf16x2(h2, h3);
-            pa[kk][3] = pack_bf16x2(p[2] - h2, p[3] - h3);
-        }
-        ps += __shfl_xor_sync(0xffffffffu, ps, 1);
-        ps += __shfl_xor_sync(0xffffffffu, ps, 2);
-        l_run = l_run * alpha + ps;
-        m_run = mn;
-#pragma unroll
-        for (int n = 0; n < DT; ++n) {
-            o[n][0] *= alpha; o[n][1] *= alpha; o[n][2] *= alpha; o[n][3] *= alpha;
-        }
-        // O += P V: V tiles read transposed (k = keys, n = dims)
-#pragma unroll
-        for (int kk = 0; kk < NT / 2; ++kk)
-#pragma unroll
-            for (int d2 = 0; d2 < DT / 2; ++d2) {
-                uint32_t v0, v1, v2, v3;
-                ldsm_x4_t(smem_u32(vs + (16 * kk + rr + ((mi & 1) << 3)) * RS + 16 * d2 + ((mi >> 1) << 3)), v0, v1, v2,
-                          v3);
-                mma_bf16(o[2 * d2], pa[kk], v0, v1);
-                mma_bf16(o[2 * d2 + 1], pa[kk], v2, v3);
             }
-        __syncthreads();   // this buffer is refilled by the next iteration's copies
+            __syncwarp();
+            if (!*ab && !mbar_wait(&kv_tma[b], (uint32_t)(j / NS) & 1u)) give_up();
+            // V rows of keys past `last` become zero
+            const int k1 = last - j0 + 1;   // keys of the tile that are <= last
+            if (!*ab && k1 < PA_KT)
+                for (int i = lane; i < (PA_KT - k1) * (HD / 8); i += PA_LOAD_T) {
+                    const int kk = k1 + i / (HD / 8), c = i % (HD / 8);
+                    *reinterpret_cast<uint4*>(vd + (c / 8) * (PA_KT * 128) + pa_sw(kk, c % 8)) = make_uint4(0u, 0u, 0u, 0u);
+                }
+            fence_proxy_async_smem();   // the zeroes (generic proxy) before the tensor core reads the tile
+            mbar_arrive(&kv_full[b]);
+        }
+    } else if (warp == 8) {
+        // ---- MMA issuer ----
+        if (lane == 0) {
+            constexpr uint32_t id_s = pf_idesc(128, PA_KT);
+            constexpr uint32_t id_o = pf_idesc(128, HD) | (1u << 16);   // B (V) MN-major
+            const uint32_t qhi = smem_u32(sm + LY::Q_HI), qlo = smem_u32(sm + LY::Q_LO);
+            const uint32_t phi = smem_u32(sm + LY::P_HI), plo = smem_u32(sm + LY::P_LO);
+            auto pv = [&](int jj) {   // O += P V of tile jj (after its P is written)
+                if (*ab || !mbar_wait(&p_full, (uint32_t)jj & 1u)) {
+                    give_up();
+                    return;
+                }
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const uint32_t vt = smem_u32(sm + LY::KV + (2 * (jj % NS) + 1) * LY::TB);
+#pragma unroll
+                for (int kk = 0; kk < PA_KT / 16; ++kk) {
+                    const uint64_t bv = pa_desc(vt + 2048u * kk, PA_KT * 128);
+                    umma_bf16(dt + 128, pa_desc(phi + 32u * kk, 16), bv, id_o, (jj > 0 || kk > 0) ? 1u : 0u);
+                    umma_bf16(dt + 128, pa_desc(plo + 32u * kk, 16), bv, id_o, 1u);
+                }
+                umma_commit(&kv_empty[jj % NS]);   // the tile's K/V stage is free
+                umma_commit(&p_free);              // P may be rewritten, O is settled
+            };
+            for (int j = 0; j < ntiles && !*ab; ++j) {
+                const int b = j & 1, kb = j % NS;   // S buffer, K/V stage
+                if (!mbar_wait(&kv_full[kb], (uint32_t)(j / NS) & 1u) ||
+                    (j >= 2 && !mbar_wait(&s_free[b], (uint32_t)((j >> 1) - 1) & 1u))) {
+                    give_up();
+                    break;
+                }
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const uint32_t kt = smem_u32(sm + LY::KV + 2 * kb * LY::TB);
+#pragma unroll
+                for (int kk = 0; kk < HD / 16; ++kk) {
+                    const uint32_t ko = (uint32_t)(kk / 4) * (PA_KT * 128) + 32u * (kk % 4);
+                    const uint32_t qo = (uint32_t)(kk / 4) * (PA_ROWS * 128) + 32u * (kk % 4);
+                    const uint64_t bk = pa_desc(kt + ko, 16);
+                    umma_bf16(dt + (uint32_t)(b * PA_KT), pa_desc(qhi + qo, 16), bk, id_s, kk > 0 ? 1u : 0u);
+                    umma_bf16(dt + (uint32_t)(b * PA_KT), pa_desc(qlo + qo, 16), bk, id_s, 1u);
+                }
+                umma_commit(&s_full[b]);
+                if (j >= 1) pv(j - 1);
+            }
+            if (!*ab) pv(ntiles - 1);
+            // every MMA issued has finished before TMEM is released (also after a give-up)
+            umma_commit(&mma_done);
+            if (!mbar_wait(&mma_done, 0u)) give_up();
+        }
+        __syncwarp();
+    } else {
+        // ---- softmax warps: warp w (0..7) reads TMEM lanes 32 (w % 4) + lane, i.e. row
+        // r = 32 (w % 4) + lane; half = w / 4 takes keys 32 half .. + 31 of each tile and
+        // O columns HD/2 half .. + HD/2 ----
+        const int quarter = warp & 3, half = warp >> 2, r = quarter * 32 + lane;
+        const int tk = t0 + r / G, qpos = pos0 + tk;
+        const bool live = tk < nt;
+        const uint32_t lrow = dt + ((uint32_t)(quarter * 32) << 16);
+        const int diag0 = pos0 + t0;   // the smallest position of the CTA's rows: earlier keys are seen by every row
+        float m_ref = -INFINITY, l = 0.f;
+        // tcgen05.ld / st are warp-wide: every condition around them is made warp-uniform
+        for (int j = 0; j < ntiles; ++j) {
+            const int b = j & 1, j0 = j * PA_KT + 32 * half;   // this thread's first key of the tile
+            bool ok = __all_sync(0xffffffffu, !*ab && mbar_wait(&s_full[b], (uint32_t)(j >> 1) & 1u));
+            if (!ok) give_up();
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            uint32_t sv[32];
+            if (ok) {
+                tmem_ld_x32(lrow + (uint32_t)(b * PA_KT + 32 * half), sv);
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+            }
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            mbar_arrive(&s_free[b]);
+            const bool all_seen = j * PA_KT + PA_KT - 1 <= diag0;   // CTA-uniform: no key of the tile is masked
+            // this half's max over the visible keys (masked keys by select), then the row's
+            float mt = -INFINITY;
+#pragma unroll
+            for (int t = 0; t < 32; ++t)
+                if (all_seen || j0 + t <= qpos) mt = fmaxf(mt, __uint_as_float(sv[t]));
+            pmax[b][half][r] = mt;
+            pa_pair_sync(quarter);
+            mt = fmaxf(mt, pmax[b][half ^ 1][r]);
+            // a new reference max when the row's max grows by more than PA_RESCALE
+            const bool need = mt > m_ref + PA_RESCALE || m_ref == -INFINITY;
+            const float mn = need ? fmaxf(mt, m_ref) : m_ref;
+            const float alpha = (need && m_ref != -INFINITY && mn != -INFINITY) ? pa_exp2(m_ref - mn) : 1.f;
+            l *= alpha;
+            m_ref = mn;
+            // P = 2^(s - m_ref) as bf16 hi and lo rows, in registers while P V of tile j - 1 runs
+            float ps = 0.f;
+            uint4 ph[4], pl[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float pv2[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int col = 8 * c + 2 * e + u;
+                        const float sc = __uint_as_float(sv[col]);
+                        pv2[u] = ((all_seen || j0 + col <= qpos) && m_ref != -INFINITY) ? pa_exp2(sc - m_ref) : 0.f;
+                        ps += pv2[u];
+                    }
+                    const float h0 = bf16_round_f(pv2[0]), h1 = bf16_round_f(pv2[1]);
+                    hi[e] = pack_bf16x2(h0, h1);
+                    lo[e] = pack_bf16x2(pv2[0] - h0, pv2[1] - h1);
+                }
+                ph[c] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                pl[c] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            }
+            l += ps;
+            // P(j - 1) has been consumed (and O settled) before P or O is touched
+            if (j >= 1 && ok) {
+                ok = __all_sync(0xffffffffu, !*ab && mbar_wait(&p_free, (uint32_t)(j - 1) & 1u));
+                if (!ok) give_up();
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            }
+            if (ok && j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {   // O holds tiles 0 .. j - 1
+#pragma unroll
+                for (int c = 0; c < HD / 2; c += 32) {
+                    uint32_t ov[32];
+                    tmem_ld_x32(lrow + 128u + (uint32_t)(half * (HD / 2) + c), ov);
+                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) ov[t] = __float_as_uint(__uint_as_float(ov[t]) * alpha);
+                    tmem_st_x32(lrow + 128u + (uint32_t)(half * (HD / 2) + c), ov);
+                }
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                *reinterpret_cast<uint4*>(sm + LY::P_HI + pa_sw(r, 4 * half + c)) = ph[c];
+                *reinterpret_cast<uint4*>(sm + LY::P_LO + pa_sw(r, 4 * half + c)) = pl[c];
+            }
+            fence_proxy_async_smem();   // P's generic writes before the tensor core reads them
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            mbar_arrive(&p_full);
+        }
+        // O / l after the last P V (the row's own position is always visible: l > 0)
+        psum[half][r] = l;
+        pa_pair_sync(quarter);
+        const float inv = 1.0f / (psum[0][r] + psum[1][r]);
+        const bool ok = __all_sync(0xffffffffu, !*ab && mbar_wait(&p_free, (uint32_t)(ntiles - 1) & 1u));
+        if (!ok) give_up();
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+#pragma unroll
+        for (int c = 0; c < HD / 2; c += 32) {
+            uint32_t ov[32];
+            tmem_ld_x32(lrow + 128u + (uint32_t)(half * (HD / 2) + c), ov);
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+            if (ok && live) {
+                const int head = g * G + r % G;
+#pragma unroll
+                for (int t = 0; t < 32; t += 4)
+                    put_hilo4(hb, qd, tk, head * HD + half * (HD / 2) + c + t,
+                              make_float4(__uint_as_float(ov[t]) * inv, __uint_as_float(ov[t + 1]) * inv,
+                                          __uint_as_float(ov[t + 2]) * inv, __uint_as_float(ov[t + 3]) * inv));
+            }
+        }
     }
-    if (!live) return;
-    // O of row gq = its bf16-part row + its remainder row
-    const float inv = 1.0f / l_run;   // the row's own position is always visible: l_run > 0
-#pragma unroll
-    for (int n = 0; n < DT; ++n)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) put_hilo(hb, qd, tok, head * HD + 8 * n + 2 * tq + e, (o[n][e] + o[n][2 + e]) * inv);
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (warp == 0) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 256;" ::"r"(dt) : "memory");
+    }
 }
 
 // rows of zeros for the hi/lo activation rows past the pass's tokens (the
@@ -467,6 +671,7 @@ struct PrefillState {
     int* pages = nullptr;
     std::vector<PfProj> proj;   // per layer: qkv, o, gate/up, down
     size_t part_floats = 0;
+    CUtensorMap* kvmaps = nullptr;   // device [L][K, V]: the attention's TMA maps of the K/V stores
 };
 
 // the partial-sum buffer: the largest splits x token rows x N over the
@@ -495,6 +700,7 @@ bool prefill_supported(const PrefillArgs& a) {
     if (G != 2 && G != 4) return false;
     if (a.d % PF_BK || qd % PF_BK || a.F % PF_BK) return false;
     if (a.d > 4 * PF_NT * PF_RN) return false;   // the norm kernel's row in registers
+    if (a.paged && (a.page < 8 || 64 % a.page)) return false;   // whole 8-row swizzle atoms per page box
     return true;
 }
 
@@ -507,16 +713,17 @@ void prefill_free(PrefillState* s) {
     cudaFree(s->hb2);
     cudaFree(s->tok);
     cudaFree(s->pages);
+    cudaFree(s->kvmaps);
     delete s;
 }
 
 static const void* pf_attn_fn(int hd, int G) {
     if (hd == 128) {
-        if (G == 4) return (const void*)&k_pf_attn_mma<128, 4>;
-        if (G == 2) return (const void*)&k_pf_attn_mma<128, 2>;
+        if (G == 4) return (const void*)&k_pf_attn_tc<128, 4>;
+        if (G == 2) return (const void*)&k_pf_attn_tc<128, 2>;
     } else if (hd == 64) {
-        if (G == 4) return (const void*)&k_pf_attn_mma<64, 4>;
-        if (G == 2) return (const void*)&k_pf_attn_mma<64, 2>;
+        if (G == 4) return (const void*)&k_pf_attn_tc<64, 4>;
+        if (G == 2) return (const void*)&k_pf_attn_tc<64, 2>;
     }
     return nullptr;
 }
@@ -537,7 +744,8 @@ cudaError_t prefill_create(const PrefillArgs& a, int num_sms, PrefillState** out
         (e = cudaMalloc(&s->hb, sizeof(__nv_bfloat16) * hrows * kmax)) != cudaSuccess ||
         (e = cudaMalloc(&s->hb2, sizeof(__nv_bfloat16) * hrows * a.F)) != cudaSuccess ||
         (e = cudaMalloc(&s->tok, sizeof(int) * a.cap)) != cudaSuccess ||
-        (e = cudaMalloc(&s->pages, sizeof(int) * (a.paged ? a.ppr : 1))) != cudaSuccess) {
+        (e = cudaMalloc(&s->pages, sizeof(int) * (a.paged ? a.ppr : 1))) != cudaSuccess ||
+        (e = cudaMalloc(&s->kvmaps, sizeof(CUtensorMap) * 2 * a.L)) != cudaSuccess) {
         cudaGetLastError();
         prefill_free(s);
         return e;
@@ -609,9 +817,25 @@ cudaError_t prefill_create(const PrefillArgs& a, int num_sms, PrefillState** out
         s->proj[4 * l + 1].add = true;
         s->proj[4 * l + 3].add = true;
     }
+    // the attention's K/V tensor maps, one pair per layer
+    {
+        std::vector<CUtensorMap> km((size_t)2 * a.L);
+        const long long kvrows = a.paged ? (long long)a.num_pages * a.Hkv * a.page : (long long)a.rows * a.Hkv * a.cap;
+        const int box = a.paged ? a.page : PA_KT;
+        for (int l = 0; l < a.L; ++l)
+            if (!pf_map(&km[2 * l], a.K[l], kvrows, a.hd, box) || !pf_map(&km[2 * l + 1], a.V[l], kvrows, a.hd, box)) {
+                prefill_free(s);
+                return cudaErrorInvalidValue;
+            }
+        if ((e = cudaMemcpy(s->kvmaps, km.data(), km.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice)) !=
+            cudaSuccess) {
+            prefill_free(s);
+            return e;
+        }
+    }
     if ((e = cudaFuncSetAttribute(k_pf_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, PF_SMEM)) != cudaSuccess ||
         (e = cudaFuncSetAttribute(pf_attn_fn(a.hd, a.Hq / a.Hkv), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  pf_attn_smem(a.hd))) != cudaSuccess) {
+                                  pf_attn_tc_smem(a.hd))) != cudaSuccess) {
         prefill_free(s);
         return e;
     }
@@ -662,10 +886,13 @@ cudaError_t prefill_run(PrefillState* s, const int* tokens, int n, int pos0, int
             k_pf_qkv<<<nt, PF_NT, 0, st>>>(s->part, sp, ntp, a.Hq, nt, p0, a.rope, s->q, kv);
             if (nt < ntp) k_pf_zero_rows<<<ntp - nt, PF_NT, 0, st>>>(s->hb, qd, nt);
             {
-                void* args[] = {&s->q, const_cast<int*>(&a.Hq), &nt, &p0, const_cast<float*>(&scale), &kv, &s->hb};
-                const int tpc = PF_QR / G;   // tokens per attention CTA
-                if ((e = cudaLaunchKernel(attn, dim3((nt + tpc - 1) / tpc, a.Hkv), dim3(256), args,
-                                          pf_attn_smem(a.hd), st)) != cudaSuccess)
+                unsigned* errp = a.err;
+                const CUtensorMap* kvm = s->kvmaps + 2 * l;
+                void* args[] = {&s->q,   const_cast<int*>(&a.Hq), &nt,   &p0, const_cast<float*>(&scale),
+                                &kv,     &kvm,                    &errp, &s->hb};
+                const int tpc = PA_ROWS / G;   // tokens per attention CTA
+                if ((e = cudaLaunchKernel(attn, dim3(a.Hkv, (nt + tpc - 1) / tpc), dim3(PA_THREADS), args,
+                                          pf_attn_tc_smem(a.hd), st)) != cudaSuccess)
                     return e;
             }
             if ((e = pf_gemm_launch(s, s->proj[4 * l + 1], nb, &sp, st)) != cudaSuccess) return e;

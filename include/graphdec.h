@@ -320,8 +320,8 @@ int dec_prefill(dec_handle *h, const int32_t *pages, const int32_t *tokens, int3
  * Positions before pos0 must already hold the sequence's K/V (from steps or an
  * earlier prefill).  Any capture with bf16 weights and K/V whose shape has
  * head_dim 64 or 128, n_heads / n_kv_heads of 2 or 4, d_model, n_heads *
- * head_dim and ffn_hidden multiples of 64 and d_model <= 8192
- * (DEC_E_UNSUPPORTED otherwise).  The
+ * head_dim and ffn_hidden multiples of 64, d_model <= 8192 and (paged
+ * K/V) pages of at least 8 tokens (DEC_E_UNSUPPORTED otherwise).  The
  * first call allocates the block's device buffers (cudaMalloc, kept until
  * dec_destroy); the call is synchronous (bounded wait) and must not be
  * captured.  Results agree with stepping the tokens one at a time within the
