@@ -422,7 +422,7 @@ def prefill_leg(dec, wl, n_tokens, reps=3) -> dict:
             "mma_tflops": round(executed / (ms * 1e-3) / 1e12, 2),
             "mma_frac_of_bf16_peak": round(executed / (ms * 1e-3) / 1e12 / peak, 4), "bf16_peak_tflops": peak,
             "note": "whole dec_prefill_block call (projections, attention, norms, K/V writes, head); "
-                    "attention runs on the tensor cores too (mma.sync, bf16 hi/lo queries), "
+                    "attention runs on the tensor cores too (tcgen05, bf16 hi/lo Q and P), "
                     "its work not counted in the TFLOP/s figures"}
 
 
