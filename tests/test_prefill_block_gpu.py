@@ -68,6 +68,19 @@ def test_prefill_block_paged_two_blocks_and_a_row():
     dec.close()
 
 
+def test_prefill_block_8b_shape_paged():
+    # head_dim 128 over a random page table: the attention's per-page TMA boxes
+    wl = gen.WORKLOADS["8b"].replace(name="8b_pfbp", n_layers=1, cap=512, vocab=2048, positions=(), layout="paged",
+                                     page_size=16, num_pages=48)
+    dec, mw = make_decoder(wl)
+    perm = gen.permutation(wl.seed, 35, wl.num_pages)
+    pages = perm[: wl.cap // wl.page_size].copy()
+    toks = gen.prompt_tokens(wl, n=300)
+    logits, pick = dec.prefill_block(toks, 0, pages=pages)
+    _check(dec, wl, mw, toks, logits, pick, pages=pages, what="8B-shape paged prefill")
+    dec.close()
+
+
 def test_prefill_block_1024_tokens():
     wl = gen.WORKLOADS["1b"].replace(name="1b_pfb1k", n_layers=2, cap=1024, vocab=2048)
     dec, mw = make_decoder(wl)
