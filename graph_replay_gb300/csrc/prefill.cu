@@ -218,8 +218,8 @@ __global__ void k_pf_qkv(const float* part, int splits, int ntp, int Hq, int nt,
 //                    buffers, so the next tile's S is computed while this one
 //                    is in softmax).  Q carries 1 / sqrt(hd) * log2(e), so
 //                    the softmax works in powers of two
-//   softmax          two threads per row (warps w and w + 4 share TMEM lanes),
-//                    32 keys each: the row's tile max through shared memory,
+//   softmax          four threads per row (warps w, w + 4, w + 8, w + 12 share
+//                    TMEM lanes), 16 keys each: the row's tile max through shared memory,
 //                    p = 2^(s - m) against the row's reference max m, the sum;
 //                    P as bf16 hi + lo rows in shared memory.  The accumulated
 //                    O and l are rescaled (O in TMEM, each thread its half of
@@ -230,13 +230,15 @@ __global__ void k_pf_qkv(const float* part, int splits, int ntp, int Hq, int nt,
 // K/V tiles arrive by TMA (128-byte swizzle: the layout the MMAs read; one box
 // per 64 keys x 64 dims, or per page x 64 dims) in a ring of stages; the
 // loader warp then zeroes the V rows past the CTA's last position (they may
-// hold any bits, and P = 0 does not clear a NaN).  Warp 8 issues the MMAs.
+// hold any bits, and P = 0 does not clear a NaN).  Warp 16 issues the MMAs.
 // All waits are bounded; one that gives up sets FAULT_WAIT and every role
 // skips the rest.
 constexpr int PA_ROWS = 128;
 constexpr int PA_KT = 64;
-constexpr int PA_SMX = 256;                // softmax threads: warps 0-7
-constexpr int PA_THREADS = PA_SMX + 64;    // + warp 8 (MMA) + warp 9 (K/V loads)
+constexpr int PA_PARTS = 4;                // softmax threads per row
+constexpr int PA_SMX = 128 * PA_PARTS;     // softmax threads: warps 0-15
+constexpr int PA_THREADS = PA_SMX + 64;    // + warp 16 (MMA) + warp 17 (K/V loads)
+constexpr int PA_MMA_WARP = PA_SMX / 32, PA_LOAD_WARP = PA_MMA_WARP + 1;
 constexpr int PA_LOAD_T = 32;
 constexpr float PA_RESCALE = 8.0f;         // log2 units: p <= 2^8 between rescales
 constexpr float PA_LOG2E = 1.4426950408889634f;
@@ -280,9 +282,34 @@ __device__ __forceinline__ void tmem_st_x32(uint32_t taddr, const uint32_t (&r)[
         "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
         : "memory");
 }
-// the two softmax warps of a TMEM lane quarter (w and w + 4) meet at barrier 1 + w
-__device__ __forceinline__ void pa_pair_sync(int quarter) {
-    asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
+// the softmax warps of a TMEM lane quarter (w, w + 4, ...) meet at barrier 1 + w
+__device__ __forceinline__ void pa_part_sync(int quarter) {
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + quarter), "n"(32 * PA_PARTS) : "memory");
+}
+__device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+template <int N>
+__device__ __forceinline__ void tmem_ld_n(uint32_t taddr, uint32_t (&r)[N]) {
+    if constexpr (N == 16) tmem_ld_x16(taddr, r);
+    else tmem_ld_x32(taddr, r);
+}
+template <int N>
+__device__ __forceinline__ void tmem_st_n(uint32_t taddr, const uint32_t (&r)[N]) {
+    if constexpr (N == 16) tmem_st_x16(taddr, r);
+    else tmem_st_x32(taddr, r);
 }
 
 // kvm: this layer's K and V tensor maps (contiguous: rows (row Hkv + g) cap + pos,
@@ -299,8 +326,8 @@ __global__ void __launch_bounds__(PA_THREADS, 1) k_pf_attn_tc(const float* q, in
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(pa_raw) + 1023) & ~(uintptr_t)1023);
     __shared__ __align__(8) uint64_t kv_tma[LY::NS], kv_full[LY::NS], kv_empty[LY::NS], s_full[2], s_free[2], p_full,
         p_free, mma_done;
-    __shared__ float pmax[2][2][PA_ROWS];   // [tile parity][half][row]: the halves' tile maxima
-    __shared__ float psum[2][PA_ROWS];      // [half][row]: the halves' sums at the end
+    __shared__ float pmax[2][PA_PARTS][PA_ROWS];   // [tile parity][part][row]: the parts' tile maxima
+    __shared__ float psum[PA_PARTS][PA_ROWS];      // [part][row]: the parts' sums at the end
     __shared__ uint32_t tmem;
     __shared__ int aborted;
     // grid (kv heads, token blocks): CTAs start in x-fastest order, so the token
@@ -379,7 +406,7 @@ __global__ void __launch_bounds__(PA_THREADS, 1) k_pf_attn_tc(const float* q, in
         atomicOr(err, FAULT_WAIT);
     };
 
-    if (warp == 9) {
+    if (warp == PA_LOAD_WARP) {
         // ---- K/V loader warp: lane 0 issues the TMA boxes, the warp zeroes late V rows ----
         for (int j = 0; j < ntiles; ++j) {
             const int b = j % NS, j0 = j * PA_KT;
@@ -424,7 +451,7 @@ __global__ void __launch_bounds__(PA_THREADS, 1) k_pf_attn_tc(const float* q, in
             fence_proxy_async_smem();   // the zeroes (generic proxy) before the tensor core reads the tile
             mbar_arrive(&kv_full[b]);
         }
-    } else if (warp == 8) {
+    } else if (warp == PA_MMA_WARP) {
         // ---- MMA issuer ----
         if (lane == 0) {
             constexpr uint32_t id_s = pf_idesc(128, PA_KT);
@@ -474,37 +501,40 @@ __global__ void __launch_bounds__(PA_THREADS, 1) k_pf_attn_tc(const float* q, in
         }
         __syncwarp();
     } else {
-        // ---- softmax warps: warp w (0..7) reads TMEM lanes 32 (w % 4) + lane, i.e. row
-        // r = 32 (w % 4) + lane; half = w / 4 takes keys 32 half .. + 31 of each tile and
-        // O columns HD/2 half .. + HD/2 ----
-        const int quarter = warp & 3, half = warp >> 2, r = quarter * 32 + lane;
+        // ---- softmax warps: warp w reads TMEM lanes 32 (w % 4) + lane, i.e. row
+        // r = 32 (w % 4) + lane; part = w / 4 takes keys KPT part .. + KPT - 1 of
+        // each tile and O columns OC part .. + OC - 1 ----
+        constexpr int KPT = PA_KT / PA_PARTS, OC = HD / PA_PARTS;
+        const int quarter = warp & 3, part = warp >> 2, r = quarter * 32 + lane;
         const int tk = t0 + r / G, qpos = pos0 + tk;
         const bool live = tk < nt;
         const uint32_t lrow = dt + ((uint32_t)(quarter * 32) << 16);
+        const uint32_t ocol = 128u + (uint32_t)(part * OC);   // this thread's O columns in TMEM
         const int diag0 = pos0 + t0;   // the smallest position of the CTA's rows: earlier keys are seen by every row
         float m_ref = -INFINITY, l = 0.f;
         // tcgen05.ld / st are warp-wide: every condition around them is made warp-uniform
         for (int j = 0; j < ntiles; ++j) {
-            const int b = j & 1, j0 = j * PA_KT + 32 * half;   // this thread's first key of the tile
+            const int b = j & 1, j0 = j * PA_KT + KPT * part;   // this thread's first key of the tile
             bool ok = __all_sync(0xffffffffu, !*ab && mbar_wait(&s_full[b], (uint32_t)(j >> 1) & 1u));
             if (!ok) give_up();
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            uint32_t sv[32];
+            uint32_t sv[KPT];
             if (ok) {
-                tmem_ld_x32(lrow + (uint32_t)(b * PA_KT + 32 * half), sv);
+                tmem_ld_n<KPT>(lrow + (uint32_t)(b * PA_KT + KPT * part), sv);
                 asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
             }
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             mbar_arrive(&s_free[b]);
             const bool all_seen = j * PA_KT + PA_KT - 1 <= diag0;   // CTA-uniform: no key of the tile is masked
-            // this half's max over the visible keys (masked keys by select), then the row's
+            // this part's max over the visible keys (masked keys by select), then the row's
             float mt = -INFINITY;
 #pragma unroll
-            for (int t = 0; t < 32; ++t)
+            for (int t = 0; t < KPT; ++t)
                 if (all_seen || j0 + t <= qpos) mt = fmaxf(mt, __uint_as_float(sv[t]));
-            pmax[b][half][r] = mt;
-            pa_pair_sync(quarter);
-            mt = fmaxf(mt, pmax[b][half ^ 1][r]);
+            pmax[b][part][r] = mt;
+            pa_part_sync(quarter);
+#pragma unroll
+            for (int o = 0; o < PA_PARTS; ++o) mt = fmaxf(mt, pmax[b][o][r]);
             // a new reference max when the row's max grows by more than PA_RESCALE
             const bool need = mt > m_ref + PA_RESCALE || m_ref == -INFINITY;
             const float mn = need ? fmaxf(mt, m_ref) : m_ref;
@@ -513,9 +543,9 @@ __global__ void __launch_bounds__(PA_THREADS, 1) k_pf_attn_tc(const float* q, in
             m_ref = mn;
             // P = 2^(s - m_ref) as bf16 hi and lo rows, in registers while P V of tile j - 1 runs
             float ps = 0.f;
-            uint4 ph[4], pl[4];
+            uint4 ph[KPT / 8], pl[KPT / 8];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < KPT / 8; ++c) {
                 uint32_t hi[4], lo[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -542,46 +572,43 @@ __global__ void __launch_bounds__(PA_THREADS, 1) k_pf_attn_tc(const float* q, in
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             }
             if (ok && j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {   // O holds tiles 0 .. j - 1
+                uint32_t ov[OC];
+                tmem_ld_n<OC>(lrow + ocol, ov);
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-                for (int c = 0; c < HD / 2; c += 32) {
-                    uint32_t ov[32];
-                    tmem_ld_x32(lrow + 128u + (uint32_t)(half * (HD / 2) + c), ov);
-                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-                    for (int t = 0; t < 32; ++t) ov[t] = __float_as_uint(__uint_as_float(ov[t]) * alpha);
-                    tmem_st_x32(lrow + 128u + (uint32_t)(half * (HD / 2) + c), ov);
-                }
+                for (int t = 0; t < OC; ++t) ov[t] = __float_as_uint(__uint_as_float(ov[t]) * alpha);
+                tmem_st_n<OC>(lrow + ocol, ov);
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             }
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                *reinterpret_cast<uint4*>(sm + LY::P_HI + pa_sw(r, 4 * half + c)) = ph[c];
-                *reinterpret_cast<uint4*>(sm + LY::P_LO + pa_sw(r, 4 * half + c)) = pl[c];
+            for (int c = 0; c < KPT / 8; ++c) {
+                *reinterpret_cast<uint4*>(sm + LY::P_HI + pa_sw(r, (KPT / 8) * part + c)) = ph[c];
+                *reinterpret_cast<uint4*>(sm + LY::P_LO + pa_sw(r, (KPT / 8) * part + c)) = pl[c];
             }
             fence_proxy_async_smem();   // P's generic writes before the tensor core reads them
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             mbar_arrive(&p_full);
         }
         // O / l after the last P V (the row's own position is always visible: l > 0)
-        psum[half][r] = l;
-        pa_pair_sync(quarter);
-        const float inv = 1.0f / (psum[0][r] + psum[1][r]);
+        psum[part][r] = l;
+        pa_part_sync(quarter);
+        float lt = 0.f;
+#pragma unroll
+        for (int o = 0; o < PA_PARTS; ++o) lt += psum[o][r];
+        const float inv = 1.0f / lt;
         const bool ok = __all_sync(0xffffffffu, !*ab && mbar_wait(&p_free, (uint32_t)(ntiles - 1) & 1u));
         if (!ok) give_up();
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        uint32_t ov[OC];
+        tmem_ld_n<OC>(lrow + ocol, ov);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        if (ok && live) {
+            const int head = g * G + r % G;
 #pragma unroll
-        for (int c = 0; c < HD / 2; c += 32) {
-            uint32_t ov[32];
-            tmem_ld_x32(lrow + 128u + (uint32_t)(half * (HD / 2) + c), ov);
-            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-            if (ok && live) {
-                const int head = g * G + r % G;
-#pragma unroll
-                for (int t = 0; t < 32; t += 4)
-                    put_hilo4(hb, qd, tk, head * HD + half * (HD / 2) + c + t,
-                              make_float4(__uint_as_float(ov[t]) * inv, __uint_as_float(ov[t + 1]) * inv,
-                                          __uint_as_float(ov[t + 2]) * inv, __uint_as_float(ov[t + 3]) * inv));
-            }
+            for (int t = 0; t < OC; t += 4)
+                put_hilo4(hb, qd, tk, head * HD + part * OC + t,
+                          make_float4(__uint_as_float(ov[t]) * inv, __uint_as_float(ov[t + 1]) * inv,
+                                      __uint_as_float(ov[t + 2]) * inv, __uint_as_float(ov[t + 3]) * inv));
         }
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
