@@ -78,7 +78,7 @@ bool compute_layout(const dec_config& c, int cap, int R, int layout, int page, i
     // persistent-kernel tables: weight and KV pointers, tensor maps, grid counters
     L->ptabs = take((size_t)c.n_layers * 11 * sizeof(void*));
     L->tmaps = take(persist_tmap_bytes(c.n_layers));
-    L->gbar = take(((size_t)kernels_per_step(c.n_layers) + 2) * sizeof(unsigned));
+    L->gbar = take(((size_t)kernels_per_step(c.n_layers) + 3) * sizeof(unsigned));
     L->dbg = take(4 * sizeof(unsigned));   // persistent kernel: wait bounds and test hooks (zero: defaults)
     L->x = take((size_t)R * d * 4);
     L->qkv = take((size_t)R * (Hq + 2 * Hkv) * hd * 4);
@@ -360,7 +360,7 @@ cudaError_t zero_state(dec_handle* h) {
         if ((e = cudaMemsetAsync(h->V[l], 0, h->lay.kv_layer, h->stream)) != cudaSuccess) return e;
     }
     if ((e = cudaMemsetAsync(h->d_status, 0, sizeof(StatusBlock), h->stream)) != cudaSuccess) return e;
-    if ((e = cudaMemsetAsync(h->ws + h->lay.gbar, 0, ((size_t)h->kernels + 2) * sizeof(unsigned), h->stream)) !=
+    if ((e = cudaMemsetAsync(h->ws + h->lay.gbar, 0, ((size_t)h->kernels + 3) * sizeof(unsigned), h->stream)) !=
         cudaSuccess)
         return e;
     if ((e = cudaMemsetAsync(h->d_slots, 0, 3 * sizeof(int32_t) * h->rows, h->stream)) != cudaSuccess) return e;

@@ -220,7 +220,7 @@ struct PersistParams {
     unsigned* err;
     unsigned long long* amax;
     unsigned* nonfinite;
-    unsigned* bar;             // [5L + 4]: per-phase arrivals, exit counter, abort word
+    unsigned* bar;             // [5L + 5]: per-phase arrivals, exit counter, abort word, head block counter
     unsigned long long* trace;
     int split_len, nsplit;
     int rps_d, rps_f;          // weight rows per ring stage for K = d and K = F

@@ -28,6 +28,14 @@
 // other wait returns at once.  The last CTA to finish resets the counters for
 // the next replay.
 //
+// Every phase but the last gives each CTA a fixed contiguous range of weight
+// rows, so that a CTA that finishes early streams the next phase's first
+// stages during the tail.  The last phase (final norm, LM head, argmax) has no
+// next phase to prefetch: its producers instead take 64 KB blocks of head rows
+// from a grid-wide counter, one take ahead, so that no SM idles while others
+// still stream.  Each row is still reduced by one CTA in slice order, so the
+// logits do not depend on which CTA took the block.
+//
 // The arithmetic of each phase is the multi-kernel graph's (gemv_impl.cuh and
 // attn_mma.cu): fixed-order reductions, no floating-point atomics, so the
 // results do not depend on scheduling.
@@ -90,6 +98,7 @@ struct PsCursor {
     const unsigned char *rs0, *rs1, *rs2;
     uint32_t rb0, rb1, rb2;
     int u, uloc, ust;          // attention: unit, stage within the unit, the unit's stages
+    int nextb;                 // head: the block taken for the next stage
 };
 
 // One stage, resolved before its ring slot is free: a GEMV stage is up to three
@@ -97,6 +106,7 @@ struct PsCursor {
 struct PsStage {
     int kind;
     int layer, u, uloc;
+    int blk;                   // head: block of head rows, -1 for the stream's end marker
     const unsigned char *s0, *s1, *s2;
     uint32_t b0, b1, b2;
 };
@@ -118,7 +128,9 @@ template <int HD, int G, int R>
 struct PsShared {
     uint64_t full_bar[PS_S];   // a ring slot's copy landed (producer's expect_tx + the copy bytes)
     uint64_t empty_bar[PS_S];  // every compute warp is done with the slot
+    int blk[PS_S];             // head phase: the block of head rows in the slot (-1: end of the stream)
     int abort;
+    int head_end;              // head phase: a compute warp met the end of the stream
     // wait bounds of this launch (the defaults unless a test shortened them) and
     // the test hooks: a phase whose grid-wait target is one above the grid size,
     // and a stage that CTA 0's producer never issues (-1: none)
@@ -131,6 +143,7 @@ struct PsShared {
         struct {
             float red[PS_RED_ROWS * R][PS_SL];   // slice partial sums of pending (weight row, decode row) pairs
             float res[PS_MAX_RES];           // residual rows (EPI_ADD)
+            int cblk[PS_RED_ROWS];           // head phase: the block of each pending stage
         } gv;
         struct {
             float q[G * HD];                 // rotated, scaled query heads of the group
@@ -195,6 +208,11 @@ struct PsState {
         return (min(j0 + P.split_len, P.cap) - j0 + PPS - 1) / PPS;
     }
 
+    // the head phase's block counter (after the phase arrivals, the exit counter
+    // and the abort word; reset with them by the last CTA out)
+    __device__ unsigned* head_ctr() const { return P.bar + np + 2; }
+    __device__ int head_blocks() const { return (P.V + P.rps_d - 1) / P.rps_d; }
+
     __device__ const CUtensorMap* tmap(int l, int which, int box) const {
         return reinterpret_cast<const CUtensorMap*>(P.tmaps) + (l * 2 + which) * 2 + box;
     }
@@ -212,6 +230,11 @@ struct PsState {
             c.u = cta;
             c.uloc = 0;
             c.ust = cta < units() ? unit_stages(cta) : 0;
+        } else if (c.kind == PK_HEAD) {
+            // blocks of rps_d rows taken from the grid-wide counter until it passes
+            // the last block; the stage after that is the end marker
+            c.nst = 0x7fffffff;
+            c.nextb = (int)atomicAdd(head_ctr(), 1u);
         } else {
             GvGeom g;
             geom(c.kind, c.layer, g);
@@ -289,6 +312,23 @@ struct PsState {
             c.nst = -1;
         }
         s.kind = c.kind;
+        if (c.kind == PK_HEAD) {
+            const int b = c.nextb;
+            if (b >= 0 && b < head_blocks()) {
+                const uint32_t rb = (uint32_t)P.d * 2u;
+                const int nr = min(P.rps_d, P.V - b * P.rps_d);
+                s.blk = b;
+                s.s0 = static_cast<const unsigned char*>(P.lm_head) + (size_t)b * P.rps_d * rb;
+                s.b0 = (uint32_t)nr * rb;
+                // the next take: its result is first used after this stage's slot wait
+                c.nextb = (int)atomicAdd(head_ctr(), 1u);
+            } else {
+                s.blk = -1;   // the end marker is the stream's last stage
+                c.p = np;
+            }
+            ++c.loc;
+            return true;
+        }
         if (c.kind == PK_ATTN) {
             s.layer = c.layer;
             s.u = c.u;
@@ -312,6 +352,17 @@ struct PsState {
     __device__ void issue(const PsStage& s, int slot) const {
         unsigned char* dst = ring + (size_t)slot * PS_SLOT;
         uint64_t* bar = &sh.full_bar[slot];
+        if (s.kind == PK_HEAD) {
+            // the header before the arrival that releases it to the consumers
+            sh.blk[slot] = s.blk;
+            if (s.blk < 0) {
+                mbar_arrive(bar);
+            } else {
+                mbar_arrive_expect_tx(bar, s.b0);
+                bulk_g2s(dst, s.s0, s.b0, bar);
+            }
+            return;
+        }
         if (s.kind != PK_ATTN) {
             mbar_arrive_expect_tx(bar, s.b0 + s.b1 + s.b2);
             if (s.b0) bulk_g2s(dst, s.s0, s.b0, bar);
@@ -546,13 +597,9 @@ __device__ __forceinline__ void ps_gemv(PsState<HD, G, PAGED, R>& st, const GvGe
         nonfin[r] = false;
     }
     bool live_all = true;
-    int c0 = 0;   // first row (within the CTA's rows) of the pending chunk
-    for (int k = 0; k < nst; ++k) {
-        const int a = k * rps;   // first row of the stage, within the CTA's rows
-        const int nr = min(rps, row1 - row0 - a);
-        const unsigned char* stg = st.stage_wait();
-        const bool live = !*reinterpret_cast<volatile int*>(&sh.abort);
-        live_all = live_all && live;
+    // one landed stage of nr weight rows: the slice partial of each (row, decode
+    // row) pair goes to the pending rows from `base` on
+    auto consume = [&](const unsigned char* stg, int nr, int base, bool live) {
         for (int m0 = 0; m0 < nr; m0 += RU) {
             float acc[RS], acc2[RS];   // sum u * R + r: weight row m0 + u, decode row r
 #pragma unroll
@@ -604,8 +651,72 @@ __device__ __forceinline__ void ps_gemv(PsState<HD, G, PAGED, R>& st, const GvGe
             int ru;
             const float t = rows_reduce<RS>(acc, lane, ru);   // ru = u * R + r
             if ((lane & (32 / RS - 1)) == 0 && m0 + ru / R < nr)
-                sh.sc.gv.red[(a - c0 + m0) * R + ru][slice] = t;
+                sh.sc.gv.red[(base + m0) * R + ru][slice] = t;
         }
+    };
+    // the argmax key and non-finite flag of a head row's logit
+    auto pick = [&](float t, int row, int r) {
+#pragma unroll
+        for (int q = 0; q < R; ++q)
+            if (q == r) {
+                if (!isfinite(t)) nonfin[q] = true;
+                const unsigned long long key = argmax_key(t, row);
+                best[q] = key > best[q] ? key : best[q];
+            }
+    };
+
+    if (EPI == EPI_LOGITS) {
+        // blocks of rps rows in the order the producer took them; a chunk of
+        // stages is flushed when full or at the end of the stream.  The compute
+        // warps see the same headers, so they agree on every chunk; a warp that
+        // stops on an abort sets head_end, which every warp reads between the
+        // chunk's two barriers, so all leave after the same chunk.
+        const int spc = PS_RED_ROWS / rps;   // stages per chunk
+        for (;;) {
+            int n = 0;
+            bool end = false;
+            for (; n < spc; ++n) {
+                const int slot = st.cons % PS_S;
+                const unsigned char* stg = st.stage_wait();
+                const bool live = !*reinterpret_cast<volatile int*>(&sh.abort);
+                live_all = live_all && live;
+                const int blk = live ? *reinterpret_cast<volatile int*>(&sh.blk[slot]) : -1;
+                if (blk < 0) {
+                    end = true;
+                    break;
+                }
+                if (tid == 0) sh.sc.gv.cblk[n] = blk;
+                consume(stg, min(rps, g.N - blk * rps), n * rps, true);
+                st.stage_release();
+            }
+            if (end && lane == 0) *reinterpret_cast<volatile int*>(&sh.head_end) = 1;
+            ST::csync();
+            const bool stop = *reinterpret_cast<volatile int*>(&sh.head_end) != 0;
+            if (live_all) {
+                for (int ir = tid; ir < n * rps * R; ir += PS_CT) {
+                    const int i = ir / R, r = ir % R;
+                    const int row = sh.sc.gv.cblk[i / rps] * rps + i % rps;
+                    if (row >= g.N) continue;
+                    float t = 0.f;
+#pragma unroll
+                    for (int w = 0; w < PS_SL; ++w) t += sh.sc.gv.red[i * R + r][w];
+                    out[(size_t)r * ostride + row] = t;
+                    pick(t, row, r);
+                }
+            }
+            ST::csync();
+            if (stop) break;
+        }
+    }
+
+    int c0 = 0;   // first row (within the CTA's rows) of the pending chunk
+    for (int k = 0; EPI != EPI_LOGITS && k < nst; ++k) {
+        const int a = k * rps;   // first row of the stage, within the CTA's rows
+        const int nr = min(rps, row1 - row0 - a);
+        const unsigned char* stg = st.stage_wait();
+        const bool live = !*reinterpret_cast<volatile int*>(&sh.abort);
+        live_all = live_all && live;
+        consume(stg, nr, a - c0, live);
         st.stage_release();
         // a full chunk (or the phase's last rows): add the slices, write the rows
         const int done = a + nr;
@@ -635,15 +746,6 @@ __device__ __forceinline__ void ps_gemv(PsState<HD, G, PAGED, R>& st, const GvGe
                         *o = (res_local ? sh.sc.gv.res[row - row0] : __ldcg(o)) + t;
                     } else {
                         *o = t;
-                    }
-                    if (EPI == EPI_LOGITS) {
-#pragma unroll
-                        for (int q = 0; q < R; ++q)
-                            if (q == r) {
-                                if (!isfinite(t)) nonfin[q] = true;
-                                const unsigned long long key = argmax_key(t, row);
-                                best[q] = key > best[q] ? key : best[q];
-                            }
                     }
                 }
             }
@@ -1008,6 +1110,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) k_persist(const __grid_constant
             mbar_init(&sh.empty_bar[s], PS_CW);
         }
         sh.abort = 0;
+        sh.head_end = 0;
         // the wait bounds and test hooks of this launch (all zero: defaults, no hooks)
         const uint4 dbg = __ldcg(reinterpret_cast<const uint4*>(P.dbg));
         sh.spin = dbg.x ? dbg.x : PS_SPIN;
@@ -1102,7 +1205,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) k_persist(const __grid_constant
         __threadfence();
         const unsigned prev = atomicAdd(P.bar + np, 1u);
         if (prev == (unsigned)gridDim.x - 1u) {
-            for (int p = 0; p <= np + 1; ++p) P.bar[p] = 0u;
+            for (int p = 0; p <= np + 2; ++p) P.bar[p] = 0u;
             for (int i = 0; i < P.R * P.Hkv; ++i) P.counters[i] = 0u;
             __threadfence();
         }
